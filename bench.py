@@ -1,0 +1,407 @@
+"""Benchmark of the NVFP4 MoE expert layer on GB300 (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one forward of the whole layer (routing, up GEMV/GEMM with relu^2,
+down GEMV/GEMM, WeightedRowSum) over one batch of the seeded synthetic
+workload, inputs already resident in HBM.  The default workload is decode-1
+(1 token, H 2688, I 1856, 128 experts, top-6); other workloads are available
+with --workload.  Between timed steps a 256 MB write flushes the 129 MB L2 and
+the routing rotates over 8 seeded variants, so weights stream from HBM.  Each
+step is bracketed by CUDA events on the launching stream; the forward is
+replayed from a CUDA graph (--no-graph launches it directly).
+
+Multi-GPU (torchrun): the layer does not shard across GPUs here, so every
+rank runs an independent replica on its own GPU (weak scaling, no data-path
+collective); rank 0 reports max-over-ranks time and the summed throughput.
+
+--impl reference times the fp64 CPU oracle (the only other implementation of
+the layer) on the host cores, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from nvfp4_quantized_moe_topk_gb300 import workload as W  # noqa: E402
+
+METRIC = "MoE layer tokens/s (decode & prefill) on 1 GB300; % of HBM / bf16 roofline"
+N_ROUTINGS = 8
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--workload", default="decode-1", choices=sorted(W.CONFIGS))
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-graph", action="store_true")
+    p.add_argument("--gemv-max-rows", type=int, default=0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    return p.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------- work model
+def algorithmic_work(wl, ids_list, T):
+    """Per-kernel algorithmic bytes / flops of one forward, averaged over the routings.
+
+    GEMV kernels: bytes = NVFP4 weights of the experts they serve (codes + block
+    scales, each read once) + activations read + outputs written.  GEMM kernels:
+    flops = 2 * rows * N * K over the rows they serve.  Combine: dst read+write,
+    k fp32 rows per token read, ids/weights read.
+    """
+    H, I, E, k, n = wl.H, wl.I, wl.E, wl.k, wl.n
+    per = {"gemv_up": [0.0, 0.0], "gemv_down": [0.0, 0.0], "gemm_up": [0.0, 0.0], "gemm_down": [0.0, 0.0],
+           "combine": [0.0, 0.0], "routing": [0.0, 0.0], "gather": [0.0, 0.0]}
+    mat_bytes = H * I // 2 + H * I // 16
+    gemm_path = n > T
+    for ids in ids_list:
+        c = np.bincount(ids.ravel(), minlength=E)
+        for e in range(E):
+            if c[e] == 0:
+                continue
+            if gemm_path and c[e] > T:
+                per["gemm_up"][1] += 2.0 * c[e] * I * H
+                per["gemm_down"][1] += 2.0 * c[e] * H * I
+                per["gemm_up"][0] += mat_bytes + c[e] * (H + I) * 2
+                per["gemm_down"][0] += mat_bytes + c[e] * (I * 2 + H * 4)
+            else:
+                per["gemv_up"][0] += mat_bytes + c[e] * (H * 2 + I * 2)
+                per["gemv_down"][0] += mat_bytes + c[e] * (I * 2 + H * 4)
+                per["gemv_up"][1] += 2.0 * c[e] * I * H
+                per["gemv_down"][1] += 2.0 * c[e] * H * I
+        per["combine"][0] += n * H * 2 * 2 + n * k * H * 4 + n * k * 8
+        per["routing"][0] += n * k * 4 * 4
+        if gemm_path:
+            per["gather"][0] += n * k * H * 2 * 2
+    m = len(ids_list)
+    return {kname: (b / m, f / m) for kname, (b, f) in per.items()}
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = "index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active," \
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown," \
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap"
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+        return False
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": ["no samples"]}
+        loaded = [s for s in sm if smax is None or s > 0.3 * smax] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- CPU baseline
+def cpu_baseline(wl, seconds: float):
+    """The fp64 oracle as it stands, on this host's cores, on a bounded token sample."""
+    import oracle
+
+    n_threads = oracle.num_threads()
+    if wl.n <= 64:
+        t0 = time.perf_counter()
+        runs = 0
+        while True:
+            oracle.moe_forward(wl)
+            runs += 1
+            if time.perf_counter() - t0 >= seconds or runs >= 1000:
+                break
+        dt = time.perf_counter() - t0
+        toks = runs * wl.n
+        sample = f"whole workload ({wl.n} tokens) x {runs} runs"
+        cores = min(n_threads, wl.n)
+    else:
+        # grow a contiguous token range until the run takes about `seconds`
+        t1 = max(1, min(wl.n, n_threads))
+        while True:
+            t0 = time.perf_counter()
+            oracle.moe_forward(wl, tok_range=(0, t1))
+            dt = time.perf_counter() - t0
+            if dt >= seconds * 0.5 or t1 >= wl.n:
+                break
+            t1 = min(wl.n, max(t1 * 2, int(t1 * seconds / max(dt, 1e-3) * 0.7)))
+        toks = t1
+        sample = f"tokens [0, {t1}) of {wl.n}"
+        cores = min(n_threads, t1)
+    return {"value": toks / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample,
+            "seconds": dt}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    wl = W.generate(args.workload)
+    import oracle
+
+    oracle.build()
+    per_step = max(1.0, 10.0 / max(1, args.steps))
+    for _ in range(args.warmup):
+        cpu_baseline(wl, 0.0)
+    vals = []
+    samples = []
+    t_all = time.perf_counter()
+    for _ in range(args.steps):
+        b = cpu_baseline(wl, per_step)
+        vals.append(b["value"])
+        samples.append(b)
+    wall = time.perf_counter() - t_all
+    value = statistics.mean(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * wall / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded)",
+            "config": {"workload": args.workload, "n": wl.n, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": samples[-1]["cores"], "kind": "oracle",
+                             "sample": samples[-1]["sample"]},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ----------------------------------------------------------------- ours
+def run_ours(args):
+    import torch
+
+    from nvfp4_quantized_moe_topk_gb300 import api
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    api.load(build_if_missing=True)
+    cfg = W.CONFIGS[args.workload]
+    wl = W.generate(args.workload)
+    T = args.gemv_max_rows if args.gemv_max_rows > 0 else 32
+    routings = [(wl.topk_ids, wl.topk_weights)] + [
+        W.make_routing(wl.n, wl.E, wl.k, cfg["bias_sigma"], seed=5000 + 97 * i) for i in range(1, N_ROUTINGS)]
+
+    def d(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            a = a.view(np.int16)
+        return torch.from_numpy(a).to(dev)
+
+    layer = api.MoeLayer(wl.H, wl.I, wl.E, wl.k, wl.n, d(wl.up_codes), d(wl.up_scales), d(wl.down_codes),
+                         d(wl.down_scales), d(wl.up_global), d(wl.down_global), gemv_max_rows=args.gemv_max_rows)
+    x = d(wl.x)
+    dst = d(wl.dst)
+    ids_d = [d(r[0]) for r in routings]
+    w_d = [d(r[1]) for r in routings]
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(W.l2_flush_bytes() // 4, dtype=torch.float32, device=dev)
+
+    def fwd(i):
+        layer.forward(x, ids_d[i % N_ROUTINGS], w_d[i % N_ROUTINGS], dst, stream=stream)
+
+    graphs = None
+    with torch.cuda.stream(stream):
+        for i in range(2 * N_ROUTINGS):
+            fwd(i)
+        torch.cuda.synchronize()
+        if not args.no_graph:
+            graphs = []
+            for i in range(N_ROUTINGS):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    fwd(i)
+                graphs.append(g)
+            torch.cuda.synchronize()
+
+    def step(i):
+        if graphs is not None:
+            graphs[i % N_ROUTINGS].replay()
+        else:
+            fwd(i)
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            flush.fill_(float(i))
+            step(i)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        with ClockSampler(local) as clk:
+            t_wall = time.perf_counter()
+            for i in range(args.steps):
+                flush.fill_(float(i))
+                ev[i][0].record(stream)
+                step(i)
+                ev[i][1].record(stream)
+            torch.cuda.synchronize()
+            t_wall = time.perf_counter() - t_wall
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms = sum(step_ms) / len(step_ms)
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * wl.n / (ms / 1000.0)
+
+    # per-kernel event timing (separate pass, same inputs, no graph) -> roofline of the dominant kernel
+    layer.set_timing(True)
+    layer.kernel_times()
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            fwd(i)
+        torch.cuda.synchronize()
+    kt = layer.kernel_times()
+    layer.set_timing(False)
+    per_launch_ms = {kname: (tot / cnt if cnt else 0.0) for kname, (tot, cnt) in kt.items()}
+    work = algorithmic_work(wl, [r[0] for r in routings], T)
+    peaks = load_peaks()
+    dom = max(per_launch_ms, key=lambda kname: per_launch_ms[kname])
+    b_alg, f_alg = work.get(dom, (0.0, 0.0))
+    if dom.startswith("gemm"):
+        achieved = f_alg / (per_launch_ms[dom] / 1000.0) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"], "traffic": None}
+    else:
+        achieved = b_alg / (per_launch_ms[dom] / 1000.0) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": None}
+    roof["kernel"] = dom
+    roof["kernel_ms"] = per_launch_ms[dom]
+    roof["peak_source"] = peaks["source"]
+    layer_bytes = sum(b for kname, (b, f) in work.items())
+    layer_flops = sum(f for kname, (b, f) in work.items() if kname.startswith("gemm"))
+
+    # end to end through the public host-buffer entry point
+    xh = torch.from_numpy(wl.x.view(np.int16)).pin_memory()
+    dh = torch.from_numpy(wl.dst.view(np.int16).copy()).pin_memory()
+    ih = [torch.from_numpy(r[0]).pin_memory() for r in routings]
+    wh = [torch.from_numpy(r[1]).pin_memory() for r in routings]
+    for i in range(3):
+        layer.forward_host(xh, ih[i % N_ROUTINGS], wh[i % N_ROUTINGS], dh, stream=stream)
+    e2e_steps = max(args.steps, 10)
+    # wall time of the synchronous host-buffer call only (the L2 flush runs outside it)
+    tot = 0.0
+    for i in range(e2e_steps):
+        flush.fill_(float(i))
+        torch.cuda.synchronize()
+        t1 = time.perf_counter()
+        layer.forward_host(xh, ih[i % N_ROUTINGS], wh[i % N_ROUTINGS], dh, stream=stream)
+        tot += time.perf_counter() - t1
+    e2e_s = tot / e2e_steps
+    h2d = wl.n * wl.H * 2 * 2 + wl.n * wl.k * 8
+    d2h = wl.n * wl.H * 2
+    layer.close()
+
+    clocks = clk.summary()
+    launches_per_step = 4 + (3 if wl.n > T else 0)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, random NVFP4 weights)",
+        "config": {"workload": args.workload, "n": wl.n, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
+                   "gemv_max_rows": T, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "flushed before every step (256 MB write)", "routings": N_ROUTINGS,
+                   "graph": graphs is not None},
+        "roofline": roof,
+        "layer": {"alg_bytes": layer_bytes, "alg_gemm_flops": layer_flops,
+                  "hbm_frac_whole_layer": layer_bytes / (ms / 1000.0) / 1e9 / peaks["hbm_gbs"],
+                  "per_kernel_ms": per_launch_ms},
+        "e2e": {"value": world * wl.n / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "wall_s_timed_region": t_wall,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line))
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

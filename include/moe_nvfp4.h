@@ -1,0 +1,198 @@
+/*
+ * moe_nvfp4.h -- C ABI of libmoe_nvfp4, the NVFP4 MoE expert layer for one
+ * GB300 GPU (sm_103a).
+ *
+ * The layer (gllm pull request #91, "perf: gather tokens per MoE expert, run
+ * large NVFP4 GEMMs on bf16 tensor cores", section "What changes"): given bf16
+ * activations x[n][H] and a top-k routing (ids, weights), every (token t,
+ * slot j) pair p = t*k + j with expert e = ids[t][j] gets one row of a packed
+ * buffer grouped by expert; each expert runs up -> relu^2 -> down over only its
+ * own rows; a fixed-order weighted row sum then adds each token's k results
+ * onto the pre-filled dst:
+ *
+ *     h      = g_up[e]   * (W_up[e]   . x[t])             fp32 accumulate
+ *     a      = bf16_rne(max(h, 0)^2)                      one rounding
+ *     y      = g_down[e] * (W_down[e] . a)                fp32 result
+ *     dst[t] = bf16_rne(dst[t] + sum_{j=0..k-1} w[t][j] * y_(t,j))   j in order
+ *
+ * NVFP4 weights: W[r][c] = e2m1(code[r][c]) * e4m3(scale[r][c/16]); the
+ * per-matrix fp32 global g is applied to the product (the GEMM alpha), never
+ * folded into the bf16 weights (same page, bf16 NVFP4 GEMM).
+ *
+ * Conventions for every entry point:
+ *   - All array arguments are plain pointers.  "device" means memory the GPU
+ *     can address (cudaMalloc'd); "host" means ordinary or pinned CPU memory.
+ *   - bf16 arrays are passed as uint16_t bit patterns.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls that
+ *     take a stream only enqueue work on it and return without waiting unless
+ *     documented otherwise.
+ *   - Matrices are row-major.  Weights are [out][in] with K (= in) contiguous:
+ *       up   codes [E][I][H/2]  scales [E][I][H/16]
+ *       down codes [E][H][I/2]  scales [E][H][I/16]
+ *     Code byte i of a row holds element 2i in its low nibble and element
+ *     2i+1 in its high nibble.  Scale bytes are E4M3FN; NaN bytes (0x7F,
+ *     0xFF) are outside the contract.
+ *   - Errors: a call that returns anything but MOE_OK has enqueued nothing.
+ *     Problems only the GPU can see (an expert id outside [0, E)) set a
+ *     flag in handle-owned device memory; read it with
+ *     moe_nvfp4_get_device_error.  No entry point aborts, traps or throws.
+ *   - Shapes supported: H and I multiples of 64, 1 <= k <= 32,
+ *     1 <= E <= 1024, n <= max_tokens given at create time.
+ */
+#ifndef MOE_NVFP4_H
+#define MOE_NVFP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad enum value */
+  MOE_ERR_UNSUPPORTED = 2, /* a shape outside the supported set (see above) */
+  MOE_ERR_CAPACITY = 3,    /* n_tokens > max_tokens of the handle */
+  MOE_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed */
+  MOE_ERR_BAD_ROUTING = 5, /* device flag: an id outside [0, E) was dropped */
+  MOE_ERR_TIMEOUT = 6,     /* device flag: a bounded in-kernel wait ran out */
+  MOE_ERR_NO_DEVICE = 7    /* no usable sm_103 device */
+} moe_status;
+
+/* Device error flag bits reported by moe_nvfp4_get_device_error. */
+#define MOE_DEVFLAG_BAD_ROUTING 0x1
+#define MOE_DEVFLAG_TIMEOUT 0x2
+
+typedef void *moe_stream_t; /* a cudaStream_t */
+
+typedef struct moe_nvfp4 *moe_nvfp4_t;
+
+typedef struct moe_nvfp4_config {
+  int32_t hidden;        /* H */
+  int32_t inter;         /* I, the expert intermediate size */
+  int32_t n_experts;     /* E */
+  int32_t top_k;         /* k */
+  int32_t max_tokens;    /* largest n a forward may be called with */
+  int32_t gemv_max_rows; /* experts with at most this many rows take the
+                            weight-streaming (GEMV) path, larger ones the
+                            tensor-core grouped GEMM; <= 0 selects 32, the
+                            threshold pull request #91 names in "Results" */
+} moe_nvfp4_config;
+
+typedef struct moe_nvfp4_weights { /* device pointers, layouts as above */
+  const uint8_t *up_codes;
+  const uint8_t *up_scales;
+  const uint8_t *down_codes;
+  const uint8_t *down_scales;
+  const float *up_global;   /* [E] */
+  const float *down_global; /* [E] */
+} moe_nvfp4_weights;
+
+/* Human-readable name of a status (static storage, never NULL). */
+MOE_API const char *moe_nvfp4_status_string(moe_status status);
+
+/* Create a layer on the current CUDA device.
+ * Copies the weights into library-owned device memory (the caller may free
+ * its copies once this returns) and allocates the whole workspace for
+ * max_tokens, so that forward never allocates (pull request #91, "Results",
+ * names per-op cudaMalloc/cudaFree as the remaining host cost).  Work is
+ * enqueued on `stream`, which is synchronized before returning.
+ * Errors: MOE_ERR_INVALID_ARG (null pointer, max_tokens < 0),
+ * MOE_ERR_UNSUPPORTED (shape), MOE_ERR_NO_DEVICE, MOE_ERR_CUDA (allocation).
+ * On error *out is set to NULL and nothing stays allocated. */
+MOE_API moe_status moe_nvfp4_create(const moe_nvfp4_config *config, const moe_nvfp4_weights *weights,
+                            moe_stream_t stream, moe_nvfp4_t *out);
+
+/* Free everything the handle owns (synchronizes the device first).  NULL is a no-op. */
+MOE_API moe_status moe_nvfp4_destroy(moe_nvfp4_t handle);
+
+/* The layer on device buffers (see top of file for the arithmetic).
+ *   x            device bf16 [n][H]
+ *   topk_ids     device int32 [n][k]
+ *   topk_weights device fp32 [n][k], used as given (no renormalisation)
+ *   dst          device bf16 [n][H], read and updated in place
+ * Enqueues the routing, the expert GEMV/GEMM kernels and the combine on
+ * `stream`; no host synchronisation, no allocation, no host read of device
+ * data.  A handle's workspace serves one forward at a time: calls on one
+ * stream are ordered; concurrent streams need separate handles.  n = 0
+ * returns MOE_OK and enqueues nothing.  Results are bitwise deterministic for
+ * a given handle configuration.
+ * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_CAPACITY (n > max_tokens), MOE_ERR_CUDA. */
+MOE_API moe_status moe_nvfp4_forward(moe_nvfp4_t handle, const uint16_t *x, const int32_t *topk_ids,
+                             const float *topk_weights, uint16_t *dst, int32_t n_tokens,
+                             moe_stream_t stream);
+
+/* Same layer on HOST buffers (pinned memory gives full copy speed): copies
+ * x, ids, weights and dst to handle-owned device staging buffers, runs the
+ * forward, copies dst back and synchronizes `stream` before returning.
+ * Same arguments and errors as moe_nvfp4_forward. */
+MOE_API moe_status moe_nvfp4_forward_host(moe_nvfp4_t handle, const uint16_t *x_host, const int32_t *topk_ids_host,
+                                  const float *topk_weights_host, uint16_t *dst_host, int32_t n_tokens,
+                                  moe_stream_t stream);
+
+/* Reads and clears the handle's device error flags (MOE_DEVFLAG_* bits).
+ * Synchronizes the device. */
+MOE_API moe_status moe_nvfp4_get_device_error(moe_nvfp4_t handle, int32_t *flags);
+
+/* Copies the routing of the most recent forward into caller device buffers
+ * (any pointer may be NULL to skip it), ordered on `stream`:
+ *   counts [E], offsets [E+1], perm_pair [n*k] (pair index p of packed row r),
+ *   inv [n*k] (packed row of pair p, -1 for a dropped pair).
+ * Rows of one expert are in ascending pair order. */
+MOE_API moe_status moe_nvfp4_debug_routing(moe_nvfp4_t handle, int32_t *counts, int32_t *offsets, int32_t *perm_pair,
+                                   int32_t *inv, moe_stream_t stream);
+
+/* Copies the packed per-row intermediates of the most recent forward into
+ * caller device buffers (NULL skips): a_rows bf16 [n*k][I] (relu^2 output),
+ * y_rows fp32 [n*k][H] (down projection), ordered on `stream`. */
+MOE_API moe_status moe_nvfp4_debug_intermediates(moe_nvfp4_t handle, uint16_t *a_rows, float *y_rows,
+                                         moe_stream_t stream);
+
+/* Per-kernel CUDA-event timing of forward (off by default).  While on, each
+ * kernel launch of forward is bracketed by an event pair on its stream. */
+MOE_API moe_status moe_nvfp4_set_timing(moe_nvfp4_t handle, int32_t enable);
+
+/* Accumulated per-kernel times since timing was enabled (synchronizes).
+ * Fills up to `capacity` entries: names[i] (static strings), total_ms[i] and
+ * launches[i]; *count receives the number of kernels seen.  Resets the sums. */
+MOE_API moe_status moe_nvfp4_kernel_times(moe_nvfp4_t handle, const char **names, double *total_ms, int64_t *launches,
+                                  int32_t capacity, int32_t *count);
+
+/* Dense NVFP4 GEMM on the tensor cores (pull request #91, "What changes",
+ * bf16 NVFP4 GEMM; "Testing", TestCUDAMatMulNVFP4Exact):
+ *   C[m][j] = global * sum_c A[m][c] * W[j][c]
+ *   A       device bf16 [M][K]
+ *   codes   device u8 [N][K/2], scales device u8 [N][K/16] (layout as above)
+ *   C       device, epilogue 0: fp32 [M][N];
+ *                   epilogue 1: bf16 [M][N] holding bf16_rne(max(C, 0)^2)
+ * K must be a multiple of 64 and N of 16; M >= 0 (M = 0 enqueues nothing).
+ * The weights are unpacked exactly to bf16 in shared memory and fed to
+ * tcgen05 MMAs with fp32 accumulation in tensor memory.  Allocates nothing.
+ * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA. */
+MOE_API moe_status nvfp4_matmul(const uint16_t *A, const uint8_t *codes, const uint8_t *scales, float global, void *C,
+                        int32_t M, int32_t N, int32_t K, int32_t epilogue, moe_stream_t stream);
+
+/* Deterministic weighted row sum (pull request #91, "What changes",
+ * WeightedRowSum):
+ *   dst[i][c] = bf16_rne(dst[i][c] + sum_{j=0..k-1} w[i][j] * src[rows[i][j]][c])
+ * with the j terms added in increasing order by one fp32 fused multiply-add
+ * each, one thread per output element, no atomics.
+ *   dst device bf16 [n][cols] (in place), src device fp32 [src_rows][cols],
+ *   rows device int32 [n][k], w device fp32 [n][k].
+ * A row index outside [0, src_rows) contributes nothing.  cols must be a
+ * multiple of 8.  Errors: MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA. */
+MOE_API moe_status weighted_row_sum(uint16_t *dst, const float *src, const int32_t *rows, const float *w, int32_t n,
+                            int32_t k, int32_t cols, int32_t src_rows, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_NVFP4_H */

@@ -1,0 +1,468 @@
+// api.cu -- the C ABI of libmoe_nvfp4 (declared in include/moe_nvfp4.h).
+//
+// Host side of the layer: argument validation (every failure returns a status
+// before anything is enqueued), ownership of the weights and of one workspace
+// sized for max_tokens at create time (gllm pull request #91, "Results":
+// per-op cudaMalloc/cudaFree and a synchronisation on every op were what
+// remained of the host cost, so forward allocates nothing and never waits),
+// tensor-map construction, and the launch sequence of one forward:
+//
+//   routing -> [gather] -> up: GEMV (small experts) + [tcgen05 GEMM (large)]
+//           -> down: GEMV + [tcgen05 GEMM] -> WeightedRowSum
+//
+// chained with programmatic dependent launch so each kernel's prologue
+// overlaps its predecessor's tail.  The GEMM kernels are enqueued only when
+// some expert can exceed the GEMV threshold (n > threshold); which experts
+// take which path is decided on the device from the routing counts.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/moe_nvfp4.h"
+#include "kernels.h"
+
+namespace {
+
+using namespace moe;
+
+enum KernelId { kKRouting = 0, kKGather, kKGemvUp, kKGemmUp, kKGemvDown, kKGemmDown, kKCombine, kKCount };
+const char* const kKernelNames[kKCount] = {"routing",   "gather",    "gemv_up", "gemm_up",
+                                           "gemv_down", "gemm_down", "combine"};
+
+struct TimingSlot {
+  cudaEvent_t beg = nullptr, end = nullptr;
+  int kernel = -1;
+};
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+struct moe_nvfp4 {
+  moe_nvfp4_config cfg{};
+  int device = 0;
+  int num_sms = 0;
+  int threshold = 32;
+  // library-owned weights
+  uint8_t *up_codes = nullptr, *up_scales = nullptr, *dn_codes = nullptr, *dn_scales = nullptr;
+  float *up_g = nullptr, *dn_g = nullptr;
+  // workspace (max_tokens)
+  int32_t *counts = nullptr, *offsets = nullptr, *perm_pair = nullptr, *inv = nullptr, *err = nullptr;
+  uint16_t *Xp = nullptr, *Ap = nullptr;
+  float* Yp = nullptr;
+  // staging for forward_host
+  uint16_t *x_stage = nullptr, *dst_stage = nullptr;
+  int32_t* ids_stage = nullptr;
+  float* w_stage = nullptr;
+  // tensor maps
+  CUtensorMap tm_xp{}, tm_ap{}, tm_up_codes{}, tm_dn_codes{};
+  int32_t last_n = 0;
+  // per-kernel timing
+  bool timing = false;
+  std::vector<TimingSlot> slots;
+  size_t slot_next = 0;
+  double total_ms[kKCount] = {};
+  int64_t launches[kKCount] = {};
+};
+
+namespace {
+
+void free_handle(moe_nvfp4* h) {
+  if (!h) return;
+  void* ptrs[] = {h->up_codes, h->up_scales, h->dn_codes, h->dn_scales, h->up_g,      h->dn_g,
+                  h->counts,   h->offsets,   h->perm_pair, h->inv,      h->err,       h->Xp,
+                  h->Ap,       h->Yp,        h->x_stage,   h->dst_stage, h->ids_stage, h->w_stage};
+  for (void* p : ptrs)
+    if (p) cudaFree(p);
+  for (auto& s : h->slots) {
+    if (s.beg) cudaEventDestroy(s.beg);
+    if (s.end) cudaEventDestroy(s.end);
+  }
+  delete h;
+}
+
+moe_status check_shape(int H, int I, int E, int k) {
+  if (H <= 0 || I <= 0 || E <= 0 || k <= 0) return MOE_ERR_INVALID_ARG;
+  if (H % 64 || I % 64 || E > 1024 || k > 32) return MOE_ERR_UNSUPPORTED;
+  if (H > 4096 || I > 4096) return MOE_ERR_UNSUPPORTED;  // GEMV lane plan covers K <= 4096
+  return MOE_OK;
+}
+
+int device_sms(int dev) {
+  int sms = 0;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return sms;
+}
+
+bool is_sm103(int dev) {
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return false;
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  return major == 10 && minor == 3;
+}
+
+// Brackets one kernel launch with timing events when timing is on.
+struct TimedLaunch {
+  moe_nvfp4* h;
+  cudaStream_t s;
+  TimingSlot* slot = nullptr;
+  TimedLaunch(moe_nvfp4* h_, cudaStream_t s_, int kernel) : h(h_), s(s_) {
+    if (!h || !h->timing || h->slots.empty()) return;
+    slot = &h->slots[h->slot_next];
+    h->slot_next = (h->slot_next + 1) % h->slots.size();
+    if (slot->kernel >= 0) {  // ring wrapped: fold the old measurement in first
+      float ms = 0.f;
+      if (cudaEventSynchronize(slot->end) == cudaSuccess && cudaEventElapsedTime(&ms, slot->beg, slot->end) == cudaSuccess) {
+        h->total_ms[slot->kernel] += ms;
+        h->launches[slot->kernel] += 1;
+      }
+    }
+    slot->kernel = kernel;
+    cudaEventRecord(slot->beg, s);
+  }
+  ~TimedLaunch() {
+    if (slot) cudaEventRecord(slot->end, s);
+  }
+};
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_nvfp4_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape";
+    case MOE_ERR_CAPACITY: return "n_tokens exceeds max_tokens";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_BAD_ROUTING: return "expert id out of range (pair dropped)";
+    case MOE_ERR_TIMEOUT: return "bounded in-kernel wait timed out";
+    case MOE_ERR_NO_DEVICE: return "no sm_103 CUDA device";
+  }
+  return "unknown status";
+}
+
+moe_status moe_nvfp4_create(const moe_nvfp4_config* config, const moe_nvfp4_weights* w, moe_stream_t stream,
+                            moe_nvfp4_t* out) {
+  if (!out) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!config || !w) return MOE_ERR_INVALID_ARG;
+  if (!w->up_codes || !w->up_scales || !w->down_codes || !w->down_scales || !w->up_global || !w->down_global)
+    return MOE_ERR_INVALID_ARG;
+  const moe_nvfp4_config c = *config;
+  moe_status st = check_shape(c.hidden, c.inter, c.n_experts, c.top_k);
+  if (st != MOE_OK) return st;
+  if (c.max_tokens < 0) return MOE_ERR_INVALID_ARG;
+  if ((long long)c.max_tokens * c.top_k > (1ll << 30)) return MOE_ERR_UNSUPPORTED;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || !is_sm103(dev)) return MOE_ERR_NO_DEVICE;
+
+  moe_nvfp4* h = new (std::nothrow) moe_nvfp4();
+  if (!h) return MOE_ERR_CUDA;
+  h->cfg = c;
+  h->device = dev;
+  h->num_sms = device_sms(dev);
+  h->threshold = c.gemv_max_rows > 0 ? c.gemv_max_rows : 32;
+  const size_t H = c.hidden, I = c.inter, E = c.n_experts;
+  const size_t R = (size_t)c.max_tokens * c.top_k, Rr = R > 0 ? R : 1;
+  const size_t mat_codes = E * H * I / 2, mat_scales = E * H * I / 16;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+#define TRY(x)                  \
+  do {                          \
+    e = (x);                    \
+    if (e != cudaSuccess) goto fail; \
+  } while (0)
+  TRY(cudaMalloc(&h->up_codes, mat_codes));
+  TRY(cudaMalloc(&h->dn_codes, mat_codes));
+  TRY(cudaMalloc(&h->up_scales, mat_scales));
+  TRY(cudaMalloc(&h->dn_scales, mat_scales));
+  TRY(cudaMalloc(&h->up_g, E * sizeof(float)));
+  TRY(cudaMalloc(&h->dn_g, E * sizeof(float)));
+  TRY(cudaMalloc(&h->counts, E * sizeof(int32_t)));
+  TRY(cudaMalloc(&h->offsets, (E + 1) * sizeof(int32_t)));
+  TRY(cudaMalloc(&h->perm_pair, Rr * sizeof(int32_t)));
+  TRY(cudaMalloc(&h->inv, Rr * sizeof(int32_t)));
+  TRY(cudaMalloc(&h->err, sizeof(int32_t)));
+  TRY(cudaMalloc(&h->Xp, Rr * H * 2));
+  TRY(cudaMalloc(&h->Ap, Rr * I * 2));
+  TRY(cudaMalloc(&h->Yp, Rr * H * 4));
+  TRY(cudaMalloc(&h->x_stage, (size_t)(c.max_tokens > 0 ? c.max_tokens : 1) * H * 2));
+  TRY(cudaMalloc(&h->dst_stage, (size_t)(c.max_tokens > 0 ? c.max_tokens : 1) * H * 2));
+  TRY(cudaMalloc(&h->ids_stage, Rr * sizeof(int32_t)));
+  TRY(cudaMalloc(&h->w_stage, Rr * sizeof(float)));
+  TRY(cudaMemcpyAsync(h->up_codes, w->up_codes, mat_codes, cudaMemcpyDeviceToDevice, s));
+  TRY(cudaMemcpyAsync(h->dn_codes, w->down_codes, mat_codes, cudaMemcpyDeviceToDevice, s));
+  TRY(cudaMemcpyAsync(h->up_scales, w->up_scales, mat_scales, cudaMemcpyDeviceToDevice, s));
+  TRY(cudaMemcpyAsync(h->dn_scales, w->down_scales, mat_scales, cudaMemcpyDeviceToDevice, s));
+  TRY(cudaMemcpyAsync(h->up_g, w->up_global, E * sizeof(float), cudaMemcpyDeviceToDevice, s));
+  TRY(cudaMemcpyAsync(h->dn_g, w->down_global, E * sizeof(float), cudaMemcpyDeviceToDevice, s));
+  TRY(cudaMemsetAsync(h->err, 0, sizeof(int32_t), s));
+  TRY(cudaMemsetAsync(h->counts, 0, E * sizeof(int32_t), s));
+  TRY(cudaMemsetAsync(h->offsets, 0, (E + 1) * sizeof(int32_t), s));
+  TRY(cudaMemsetAsync(h->Ap, 0, Rr * I * 2, s));
+  TRY(cudaMemsetAsync(h->Yp, 0, Rr * H * 4, s));
+  TRY(make_tmap_act(&h->tm_xp, h->Xp, Rr, H));
+  TRY(make_tmap_act(&h->tm_ap, h->Ap, Rr, I));
+  TRY(make_tmap_codes(&h->tm_up_codes, h->up_codes, E * I, H));
+  TRY(make_tmap_codes(&h->tm_dn_codes, h->dn_codes, E * H, I));
+  TRY(cudaStreamSynchronize(s));
+#undef TRY
+  *out = h;
+  return MOE_OK;
+fail:
+  cudaStreamSynchronize(s);
+  free_handle(h);
+  return MOE_ERR_CUDA;
+}
+
+moe_status moe_nvfp4_destroy(moe_nvfp4_t h) {
+  if (!h) return MOE_OK;
+  cudaDeviceSynchronize();
+  free_handle(h);
+  return MOE_OK;
+}
+
+static moe_status forward_impl(moe_nvfp4* h, const uint16_t* x, const int32_t* ids, const float* tw, uint16_t* dst,
+                               int32_t n, cudaStream_t s) {
+  const moe_nvfp4_config& c = h->cfg;
+  const int32_t k = c.top_k, E = c.n_experts, H = c.hidden, I = c.inter;
+  const int32_t R = n * k;
+  const bool gemm = n > h->threshold;
+  const bool pdl = !h->timing;
+  h->last_n = n;
+  cudaError_t e;
+  {
+    TimedLaunch tl(h, s, kKRouting);
+    e = launch_routing(ids, R, E, h->counts, h->offsets, h->perm_pair, h->inv, h->err, s);
+  }
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (gemm) {
+    TimedLaunch tl(h, s, kKGather);
+    e = launch_gather(x, h->perm_pair, h->offsets + E, R, k, H, h->Xp, s, pdl);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  GemvArgs g{};
+  g.counts = h->counts;
+  g.offsets = h->offsets;
+  g.perm_pair = h->perm_pair;
+  g.E = E;
+  g.k = k;
+  g.max_rows = gemm ? h->threshold : 0;
+  {
+    TimedLaunch tl(h, s, kKGemvUp);
+    g.codes = h->up_codes;
+    g.scales = h->up_scales;
+    g.global = h->up_g;
+    g.in = x;
+    g.out = h->Ap;
+    g.N = I;
+    g.K = H;
+    g.token_indexed = 1;
+    g.relu2_bf16_out = 1;
+    e = launch_gemv(g, s, pdl);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  GemmArgs m{};
+  m.counts = h->counts;
+  m.offsets = h->offsets;
+  m.G = E;
+  m.min_rows = h->threshold;
+  m.err = h->err;
+  if (gemm) {
+    TimedLaunch tl(h, s, kKGemmUp);
+    m.scales = h->up_scales;
+    m.global = h->up_g;
+    m.N = I;
+    m.K = H;
+    m.out = h->Ap;
+    m.epilogue = 1;
+    e = launch_gemm(h->tm_xp, h->tm_up_codes, m, h->num_sms, s, pdl);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  {
+    TimedLaunch tl(h, s, kKGemvDown);
+    g.codes = h->dn_codes;
+    g.scales = h->dn_scales;
+    g.global = h->dn_g;
+    g.in = h->Ap;
+    g.out = h->Yp;
+    g.N = H;
+    g.K = I;
+    g.token_indexed = 0;
+    g.relu2_bf16_out = 0;
+    e = launch_gemv(g, s, pdl);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  if (gemm) {
+    TimedLaunch tl(h, s, kKGemmDown);
+    m.scales = h->dn_scales;
+    m.global = h->dn_g;
+    m.N = H;
+    m.K = I;
+    m.out = h->Yp;
+    m.epilogue = 0;
+    e = launch_gemm(h->tm_ap, h->tm_dn_codes, m, h->num_sms, s, pdl);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  {
+    TimedLaunch tl(h, s, kKCombine);
+    e = launch_weighted_row_sum(dst, h->Yp, h->inv, tw, n, k, H, R, s, pdl);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+moe_status moe_nvfp4_forward(moe_nvfp4_t h, const uint16_t* x, const int32_t* ids, const float* tw, uint16_t* dst,
+                             int32_t n, moe_stream_t stream) {
+  if (!h || n < 0) return MOE_ERR_INVALID_ARG;
+  if (n > h->cfg.max_tokens) return MOE_ERR_CAPACITY;
+  if (n == 0) return MOE_OK;
+  if (!x || !ids || !tw || !dst) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(dst, 16) || !aligned(ids, 4) || !aligned(tw, 4)) return MOE_ERR_INVALID_ARG;
+  return forward_impl(h, x, ids, tw, dst, n, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_nvfp4_forward_host(moe_nvfp4_t h, const uint16_t* x, const int32_t* ids, const float* tw,
+                                  uint16_t* dst, int32_t n, moe_stream_t stream) {
+  if (!h || n < 0) return MOE_ERR_INVALID_ARG;
+  if (n > h->cfg.max_tokens) return MOE_ERR_CAPACITY;
+  if (n == 0) return MOE_OK;
+  if (!x || !ids || !tw || !dst) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t H = h->cfg.hidden, R = (size_t)n * h->cfg.top_k;
+  if (cudaMemcpyAsync(h->x_stage, x, (size_t)n * H * 2, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(h->ids_stage, ids, R * 4, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(h->w_stage, tw, R * 4, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(h->dst_stage, dst, (size_t)n * H * 2, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  moe_status st = forward_impl(h, h->x_stage, h->ids_stage, h->w_stage, h->dst_stage, n, s);
+  if (st != MOE_OK) return st;
+  if (cudaMemcpyAsync(dst, h->dst_stage, (size_t)n * H * 2, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return cuda_status(cudaStreamSynchronize(s));
+}
+
+moe_status moe_nvfp4_get_device_error(moe_nvfp4_t h, int32_t* flags) {
+  if (!h || !flags) return MOE_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+  int32_t v = 0;
+  if (cudaMemcpy(&v, h->err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemset(h->err, 0, sizeof(int32_t)) != cudaSuccess) return MOE_ERR_CUDA;
+  *flags = v;
+  return MOE_OK;
+}
+
+moe_status moe_nvfp4_debug_routing(moe_nvfp4_t h, int32_t* counts, int32_t* offsets, int32_t* perm_pair,
+                                   int32_t* inv, moe_stream_t stream) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t E = h->cfg.n_experts, R = (size_t)h->last_n * h->cfg.top_k;
+  cudaError_t e = cudaSuccess;
+  if (counts && e == cudaSuccess) e = cudaMemcpyAsync(counts, h->counts, E * 4, cudaMemcpyDeviceToDevice, s);
+  if (offsets && e == cudaSuccess)
+    e = cudaMemcpyAsync(offsets, h->offsets, (E + 1) * 4, cudaMemcpyDeviceToDevice, s);
+  if (perm_pair && R && e == cudaSuccess)
+    e = cudaMemcpyAsync(perm_pair, h->perm_pair, R * 4, cudaMemcpyDeviceToDevice, s);
+  if (inv && R && e == cudaSuccess) e = cudaMemcpyAsync(inv, h->inv, R * 4, cudaMemcpyDeviceToDevice, s);
+  return cuda_status(e);
+}
+
+moe_status moe_nvfp4_debug_intermediates(moe_nvfp4_t h, uint16_t* a_rows, float* y_rows, moe_stream_t stream) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t R = (size_t)h->last_n * h->cfg.top_k;
+  cudaError_t e = cudaSuccess;
+  if (a_rows && R) e = cudaMemcpyAsync(a_rows, h->Ap, R * h->cfg.inter * 2, cudaMemcpyDeviceToDevice, s);
+  if (y_rows && R && e == cudaSuccess)
+    e = cudaMemcpyAsync(y_rows, h->Yp, R * h->cfg.hidden * 4, cudaMemcpyDeviceToDevice, s);
+  return cuda_status(e);
+}
+
+moe_status moe_nvfp4_set_timing(moe_nvfp4_t h, int32_t enable) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  if (enable && h->slots.empty()) {
+    h->slots.resize(512);
+    for (auto& sl : h->slots) {
+      if (cudaEventCreate(&sl.beg) != cudaSuccess || cudaEventCreate(&sl.end) != cudaSuccess) return MOE_ERR_CUDA;
+    }
+  }
+  h->timing = enable != 0;
+  return MOE_OK;
+}
+
+moe_status moe_nvfp4_kernel_times(moe_nvfp4_t h, const char** names, double* total_ms, int64_t* launches,
+                                  int32_t capacity, int32_t* count) {
+  if (!h || !count) return MOE_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+  for (auto& sl : h->slots) {
+    if (sl.kernel < 0) continue;
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, sl.beg, sl.end) == cudaSuccess) {
+      h->total_ms[sl.kernel] += ms;
+      h->launches[sl.kernel] += 1;
+    }
+    sl.kernel = -1;
+  }
+  *count = kKCount;
+  for (int i = 0; i < kKCount && i < capacity; ++i) {
+    if (names) names[i] = kKernelNames[i];
+    if (total_ms) total_ms[i] = h->total_ms[i];
+    if (launches) launches[i] = h->launches[i];
+  }
+  for (int i = 0; i < kKCount; ++i) {
+    h->total_ms[i] = 0;
+    h->launches[i] = 0;
+  }
+  return MOE_OK;
+}
+
+moe_status nvfp4_matmul(const uint16_t* A, const uint8_t* codes, const uint8_t* scales, float global, void* C,
+                        int32_t M, int32_t N, int32_t K, int32_t epilogue, moe_stream_t stream) {
+  if (M < 0 || N <= 0 || K <= 0 || (epilogue != 0 && epilogue != 1)) return MOE_ERR_INVALID_ARG;
+  if (K % 64 || N % 16) return MOE_ERR_UNSUPPORTED;
+  if (M == 0) return MOE_OK;
+  if (!A || !codes || !scales || !C) return MOE_ERR_INVALID_ARG;
+  if (!aligned(A, 16) || !aligned(codes, 16) || !aligned(scales, 4) || !aligned(C, 16)) return MOE_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || !is_sm103(dev)) return MOE_ERR_NO_DEVICE;
+  CUtensorMap ta, tb;
+  if (make_tmap_act(&ta, A, (uint64_t)M, (uint64_t)K) != cudaSuccess) return MOE_ERR_CUDA;
+  if (make_tmap_codes(&tb, codes, (uint64_t)N, (uint64_t)K) != cudaSuccess) return MOE_ERR_CUDA;
+  GemmArgs m{};
+  m.scales = scales;
+  m.global = nullptr;
+  m.alpha0 = global;
+  m.counts = nullptr;
+  m.offsets = nullptr;
+  m.M = M;
+  m.G = 1;
+  m.N = N;
+  m.K = K;
+  m.min_rows = 0;
+  m.out = C;
+  m.epilogue = epilogue;
+  m.err = nullptr;
+  return cuda_status(launch_gemm(ta, tb, m, device_sms(dev), reinterpret_cast<cudaStream_t>(stream), false));
+}
+
+moe_status weighted_row_sum(uint16_t* dst, const float* src, const int32_t* rows, const float* w, int32_t n,
+                            int32_t k, int32_t cols, int32_t src_rows, moe_stream_t stream) {
+  if (n < 0 || k <= 0 || cols <= 0 || src_rows < 0) return MOE_ERR_INVALID_ARG;
+  if (cols % 8) return MOE_ERR_UNSUPPORTED;
+  if (n == 0) return MOE_OK;
+  if (!dst || !src || !rows || !w) return MOE_ERR_INVALID_ARG;
+  if (!aligned(dst, 16) || !aligned(src, 16) || !aligned(rows, 4) || !aligned(w, 4)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(
+      launch_weighted_row_sum(dst, src, rows, w, n, k, cols, src_rows, reinterpret_cast<cudaStream_t>(stream), false));
+}
+
+}  // extern "C"

@@ -1,0 +1,82 @@
+// kernels.h -- internal launchers of libmoe_nvfp4 (not part of the public ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+// ---------------------------------------------------------------- routing
+size_t routing_smem_bytes(int E);
+cudaError_t launch_routing(const int32_t* ids, int32_t R, int32_t E, int32_t* counts, int32_t* offsets,
+                           int32_t* perm_pair, int32_t* inv, int32_t* err, cudaStream_t s);
+
+// ------------------------------------------------------------ gather / combine
+// Xp[r][:] = x[perm_pair[r] / k][:] for r < offsets[E].
+cudaError_t launch_gather(const uint16_t* x, const int32_t* perm_pair, const int32_t* kept_rows, int32_t R,
+                          int32_t k, int32_t H, uint16_t* Xp, cudaStream_t s, bool pdl);
+// dst[i][c] = bf16(dst[i][c] + sum_j w[i][j] * src[rows[i][j]][c]), fixed j order.
+cudaError_t launch_weighted_row_sum(uint16_t* dst, const float* src, const int32_t* rows, const float* w,
+                                    int32_t n, int32_t k, int32_t cols, int32_t src_rows, cudaStream_t s,
+                                    bool pdl);
+
+// ------------------------------------------------------------ NVFP4 GEMV
+// Weight-streaming matrix-vector path for experts with few rows.
+struct GemvArgs {
+  const uint8_t* codes;    // [E][N][K/2]
+  const uint8_t* scales;   // [E][N][K/16]
+  const float* global;     // [E]
+  const int32_t* counts;   // [E]
+  const int32_t* offsets;  // [E+1]
+  const int32_t* perm_pair;  // [R] (token-indexed input only)
+  const uint16_t* in;      // bf16: x [n][K] (token-indexed) or Ap [R][K] (row-indexed)
+  void* out;               // bf16 Ap [R][N] (relu^2) or fp32 Yp [R][N]
+  int32_t E, N, K, k;
+  int32_t max_rows;        // experts with 0 < count <= max_rows take this path (<= 0: every expert)
+  int32_t token_indexed;   // 1: input row of packed row r is in[perm_pair[r] / k]
+  int32_t relu2_bf16_out;  // 1: out = bf16(max(g*acc,0)^2); 0: out = fp32 g*acc
+};
+cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t s, bool pdl);
+
+// ------------------------------------------------------- tcgen05 grouped GEMM
+struct GemmArgs {
+  const uint8_t* scales;   // [G][N][K/16] (G groups of N weight rows)
+  const float* global;     // [G] per-group alpha, or nullptr to use alpha0
+  float alpha0;
+  const int32_t* counts;   // [G] rows per group, or nullptr: single group of M rows
+  const int32_t* offsets;  // [G+1]
+  int32_t M;               // single-group row count (counts == nullptr)
+  int32_t G, N, K;
+  int32_t min_rows;        // groups with count > min_rows take this path (grouped mode)
+  void* out;               // [rows][N]: fp32 (epilogue 0) or bf16 relu^2 (epilogue 1)
+  int32_t epilogue;
+  int32_t* err;            // device error flag (may be nullptr)
+};
+// tmA: bf16 activations [rows][K], box 64 x 128, 128-byte swizzle.
+// tmB: weight codes [G*N][K/2] bytes, box 32 x 256, no swizzle.
+cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int num_sms,
+                        cudaStream_t s, bool pdl);
+
+// Host helpers for tensor maps (driver entry point resolved at run time).
+cudaError_t make_tmap_act(CUtensorMap* map, const void* base, uint64_t rows, uint64_t K);
+cudaError_t make_tmap_codes(CUtensorMap* map, const void* base, uint64_t rows, uint64_t K);
+
+// Launch with the programmatic-stream-serialization attribute when pdl is set.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                      Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+}  // namespace moe

@@ -1,0 +1,63 @@
+"""Shared helpers for the parity tests: upload seeded workloads, compare to the oracle."""
+import numpy as np
+
+from nvfp4_quantized_moe_topk_gb300 import workload as W
+
+
+def to_dev(a, dev):
+    import torch
+
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    return torch.from_numpy(a).to(dev)
+
+
+def bf16_from_dev(t) -> np.ndarray:
+    return t.cpu().numpy().view(np.uint16)
+
+
+def make_layer(wl, dev, max_tokens=None, gemv_max_rows=0, stream=None):
+    from nvfp4_quantized_moe_topk_gb300 import api
+
+    return api.MoeLayer(wl.H, wl.I, wl.E, wl.k, wl.n if max_tokens is None else max_tokens,
+                        to_dev(wl.up_codes, dev), to_dev(wl.up_scales, dev), to_dev(wl.down_codes, dev),
+                        to_dev(wl.down_scales, dev), to_dev(wl.up_global, dev), to_dev(wl.down_global, dev),
+                        gemv_max_rows=gemv_max_rows, stream=stream)
+
+
+def run_forward(layer, wl, dev, stream=None):
+    """Upload x / ids / weights / dst, run the layer, return the new dst (bf16 bits)."""
+    import torch
+
+    x = to_dev(wl.x, dev)
+    ids = to_dev(wl.topk_ids, dev)
+    w = to_dev(wl.topk_weights, dev)
+    dst = to_dev(wl.dst, dev)
+    layer.forward(x, ids, w, dst, stream=stream)
+    torch.cuda.synchronize()
+    return bf16_from_dev(dst)
+
+
+def layer_tolerance_check(got_bits, ref_bits, rows=None):
+    """max|y - y_ref| <= 1e-2 * RMS(y_ref) on the layer output, plus one bf16 ulp of
+    the reference for the single final rounding that both sides make from
+    different-precision sums.  Returns (ok, max_err, rms)."""
+    g = W.bf16_bits_to_f32(got_bits).astype(np.float64)
+    r = W.bf16_bits_to_f32(ref_bits).astype(np.float64)
+    if rows is not None:
+        g, r = g[rows], r[rows]
+    rms = float(np.sqrt(np.mean(r * r)))
+    ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(r), 1e-30))) - 7)
+    err = np.abs(g - r)
+    ok = bool(np.all(err <= 1e-2 * rms + ulp))
+    return ok, float(err.max()), rms
+
+
+def fp_tolerance_check(got, ref):
+    """max|y - y_ref| <= 1e-2 * RMS(y_ref) for fp32 results against fp64."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    rms = float(np.sqrt(np.mean(ref * ref))) if ref.size else 0.0
+    err = float(np.max(np.abs(got - ref))) if ref.size else 0.0
+    return err <= 1e-2 * rms, err, rms
