@@ -191,6 +191,33 @@ MOE_API moe_status nvfp4_matmul(const uint16_t *A, const uint8_t *codes, const u
 MOE_API moe_status weighted_row_sum(uint16_t *dst, const float *src, const int32_t *rows, const float *w, int32_t n,
                             int32_t k, int32_t cols, int32_t src_rows, moe_stream_t stream);
 
+/* The layer for callers that cannot allocate device memory.  The pages have
+ * no counterpart of this call.  Some callers cannot call cudaMalloc: a plugin
+ * or server whose host process owns all device memory through its own pool
+ * and must account for every byte, a caller with a memory budget fixed at
+ * load time, or code that must not risk the device-wide synchronisation an
+ * allocation can cause.  This call needs no handle and allocates nothing:
+ *   config, weights  as for moe_nvfp4_create, but the weights are read in
+ *                    place from the caller's device memory on every call
+ *   x, topk_ids, topk_weights, dst, n_tokens, stream  as for moe_nvfp4_forward
+ * Every intermediate (routing arrays, relu^2 rows, down rows, error flag)
+ * lives in one file-scope device array of 8 MiB that every GPU which loads
+ * the library holds until the process exits.  A call needs
+ *   about 4*(2E + 2R) + R*(2*I + 4*H) bytes of it, R = n_tokens * top_k
+ * (for H = 2688, I = 1856, E = 128 that is up to 579 rows, 96 tokens at
+ * top-6); larger calls return
+ * MOE_ERR_CAPACITY and enqueue nothing.  The first call on a device looks up
+ * the array's device address (cudaGetSymbolAddress) and caches it: make that
+ * first call before any stream capture.  All calls on a device share the
+ * array and it keeps the last call's contents, so calls whose work overlaps
+ * on the GPU race on it; order them.  Every expert runs on the weight-
+ * streaming kernel; ids outside [0, E) are dropped (they add nothing) and
+ * are not reported.  Errors: MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED,
+ * MOE_ERR_CAPACITY, MOE_ERR_NO_DEVICE, MOE_ERR_CUDA. */
+MOE_API moe_status moe_nvfp4_forward_noalloc(const moe_nvfp4_config *config, const moe_nvfp4_weights *weights,
+                                             const uint16_t *x, const int32_t *topk_ids, const float *topk_weights,
+                                             uint16_t *dst, int32_t n_tokens, moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -24,7 +24,7 @@ DEVFLAG_TIMEOUT = 0x2
 ENTRY_POINTS = ("moe_nvfp4_status_string", "moe_nvfp4_create", "moe_nvfp4_destroy", "moe_nvfp4_forward",
                 "moe_nvfp4_forward_host", "moe_nvfp4_get_device_error", "moe_nvfp4_debug_routing",
                 "moe_nvfp4_debug_intermediates", "moe_nvfp4_set_timing", "moe_nvfp4_kernel_times",
-                "nvfp4_matmul", "weighted_row_sum")
+                "nvfp4_matmul", "weighted_row_sum", "moe_nvfp4_forward_noalloc")
 
 _lock = threading.Lock()
 _lib = None
@@ -78,6 +78,8 @@ def load(build_if_missing: bool = False):
                                              ctypes.POINTER(i64), i32, ctypes.POINTER(i32)]
         L.nvfp4_matmul.argtypes = [vp, vp, vp, ctypes.c_float, vp, i32, i32, i32, i32, vp]
         L.weighted_row_sum.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, vp]
+        L.moe_nvfp4_forward_noalloc.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(Weights), vp, vp, vp, vp,
+                                                i32, vp]
         for name in ENTRY_POINTS:
             if name != "moe_nvfp4_status_string":
                 getattr(L, name).restype = ctypes.c_int
@@ -196,4 +198,19 @@ def weighted_row_sum(dst, src, rows, w, stream=None):
     k = rows.shape[1]
     _check(load().weighted_row_sum(_ptr(dst), _ptr(src), _ptr(rows), _ptr(w), n, k, cols, src.shape[0],
                                    _stream(stream)), "weighted_row_sum")
+    return dst
+
+
+def forward_noalloc(hidden, inter, n_experts, top_k, up_codes, up_scales, down_codes, down_scales, up_global,
+                    down_global, x, topk_ids, topk_weights, dst, n_tokens: int | None = None, stream=None):
+    """``moe_nvfp4_forward_noalloc``: the layer without a handle and without any
+    device allocation (weights read in place; intermediates in the library's
+    fixed device array)."""
+    n = x.shape[0] if n_tokens is None else n_tokens
+    cfg = Config(hidden, inter, n_experts, top_k, n, 0)
+    w = Weights(_ptr(up_codes), _ptr(up_scales), _ptr(down_codes), _ptr(down_scales), _ptr(up_global),
+                _ptr(down_global))
+    _check(load().moe_nvfp4_forward_noalloc(ctypes.byref(cfg), ctypes.byref(w), _ptr(x), _ptr(topk_ids),
+                                            _ptr(topk_weights), _ptr(dst), n, _stream(stream)),
+           "moe_nvfp4_forward_noalloc")
     return dst
