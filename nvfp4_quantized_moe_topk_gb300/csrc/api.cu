@@ -30,9 +30,9 @@ namespace {
 
 using namespace moe;
 
-enum KernelId { kKRouting = 0, kKGather, kKGemvUp, kKGemmUp, kKGemvDown, kKGemmDown, kKCombine, kKCount };
+enum KernelId { kKRouting = 0, kKGather, kKGemvUp, kKGemmUp, kKGemvDown, kKGemmDown, kKCombine, kKDecode, kKCount };
 const char* const kKernelNames[kKCount] = {"routing",   "gather",    "gemv_up", "gemm_up",
-                                           "gemv_down", "gemm_down", "combine"};
+                                           "gemv_down", "gemm_down", "combine", "decode"};
 
 struct TimingSlot {
   cudaEvent_t beg = nullptr, end = nullptr;
@@ -51,6 +51,9 @@ struct moe_nvfp4 {
   // library-owned weights
   uint8_t *up_codes = nullptr, *up_scales = nullptr, *dn_codes = nullptr, *dn_scales = nullptr;
   float *up_g = nullptr, *dn_g = nullptr;
+  // the same weights in fragment-tile order for the single-launch small-batch path
+  uint8_t *up_tiles = nullptr, *dn_tiles = nullptr;
+  int32_t *col_done = nullptr, *grid_bar = nullptr;
   // workspace (max_tokens)
   int32_t *counts = nullptr, *offsets = nullptr, *perm_pair = nullptr, *inv = nullptr, *err = nullptr;
   uint16_t *Xp = nullptr, *Ap = nullptr;
@@ -76,7 +79,8 @@ void free_handle(moe_nvfp4* h) {
   if (!h) return;
   void* ptrs[] = {h->up_codes, h->up_scales, h->dn_codes, h->dn_scales, h->up_g,      h->dn_g,
                   h->counts,   h->offsets,   h->perm_pair, h->inv,      h->err,       h->Xp,
-                  h->Ap,       h->Yp,        h->x_stage,   h->dst_stage, h->ids_stage, h->w_stage};
+                  h->Ap,       h->Yp,        h->x_stage,   h->dst_stage, h->ids_stage, h->w_stage,
+                  h->up_tiles, h->dn_tiles,  h->col_done,  h->grid_bar};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   for (auto& s : h->slots) {
@@ -199,6 +203,10 @@ moe_status moe_nvfp4_create(const moe_nvfp4_config* config, const moe_nvfp4_weig
   TRY(cudaMalloc(&h->dst_stage, (size_t)(c.max_tokens > 0 ? c.max_tokens : 1) * H * 2));
   TRY(cudaMalloc(&h->ids_stage, Rr * sizeof(int32_t)));
   TRY(cudaMalloc(&h->w_stage, Rr * sizeof(float)));
+  TRY(cudaMalloc(&h->up_tiles, mat_codes + mat_scales));
+  TRY(cudaMalloc(&h->dn_tiles, mat_codes + mat_scales));
+  TRY(cudaMalloc(&h->col_done, (H / 16) * sizeof(int32_t)));
+  TRY(cudaMalloc(&h->grid_bar, 2 * sizeof(int32_t)));
   TRY(cudaMemcpyAsync(h->up_codes, w->up_codes, mat_codes, cudaMemcpyDeviceToDevice, s));
   TRY(cudaMemcpyAsync(h->dn_codes, w->down_codes, mat_codes, cudaMemcpyDeviceToDevice, s));
   TRY(cudaMemcpyAsync(h->up_scales, w->up_scales, mat_scales, cudaMemcpyDeviceToDevice, s));
@@ -210,6 +218,10 @@ moe_status moe_nvfp4_create(const moe_nvfp4_config* config, const moe_nvfp4_weig
   TRY(cudaMemsetAsync(h->offsets, 0, (E + 1) * sizeof(int32_t), s));
   TRY(cudaMemsetAsync(h->Ap, 0, Rr * I * 2, s));
   TRY(cudaMemsetAsync(h->Yp, 0, Rr * H * 4, s));
+  TRY(cudaMemsetAsync(h->col_done, 0, (H / 16) * sizeof(int32_t), s));
+  TRY(cudaMemsetAsync(h->grid_bar, 0, 2 * sizeof(int32_t), s));
+  TRY(launch_repack_frag(h->up_codes, h->up_scales, (int32_t)E, (int32_t)I, (int32_t)H, h->up_tiles, s));
+  TRY(launch_repack_frag(h->dn_codes, h->dn_scales, (int32_t)E, (int32_t)H, (int32_t)I, h->dn_tiles, s));
   TRY(make_tmap_act(&h->tm_xp, h->Xp, Rr, H));
   TRY(make_tmap_act(&h->tm_ap, h->Ap, Rr, I));
   TRY(make_tmap_codes(&h->tm_up_codes, h->up_codes, E * I, H));
@@ -240,6 +252,37 @@ static moe_status forward_impl(moe_nvfp4* h, const uint16_t* x, const int32_t* i
   const bool pdl = !h->timing;
   h->last_n = n;
   cudaError_t e;
+  if (!gemm && R <= kDecMaxPairs) {
+    const DecLayout L = decode_layout(E, R);
+    if (L.warps >= 4) {
+      DecodeArgs d{};
+      d.up_tiles = h->up_tiles;
+      d.dn_tiles = h->dn_tiles;
+      d.up_g = h->up_g;
+      d.dn_g = h->dn_g;
+      d.x = x;
+      d.ids = ids;
+      d.tw = tw;
+      d.dst = dst;
+      d.Ap = h->Ap;
+      d.Yp = h->Yp;
+      d.g_counts = h->counts;
+      d.g_offsets = h->offsets;
+      d.g_perm = h->perm_pair;
+      d.g_inv = h->inv;
+      d.col_done = h->col_done;
+      d.grid_bar = h->grid_bar;
+      d.err = h->err;
+      d.n = n;
+      d.H = H;
+      d.I = I;
+      d.E = E;
+      d.k = k;
+      d.L = L;
+      TimedLaunch tl(h, s, kKDecode);
+      return cuda_status(launch_decode(d, h->num_sms, s));
+    }
+  }
   {
     TimedLaunch tl(h, s, kKRouting);
     e = launch_routing(ids, R, E, h->counts, h->offsets, h->perm_pair, h->inv, h->err, s);
@@ -357,6 +400,11 @@ moe_status moe_nvfp4_get_device_error(moe_nvfp4_t h, int32_t* flags) {
   int32_t v = 0;
   if (cudaMemcpy(&v, h->err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaMemset(h->err, 0, sizeof(int32_t)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (v & MOE_DEVFLAG_TIMEOUT) {  // a wait gave up: the cross-CTA counters may be left mid-count
+    if (cudaMemset(h->col_done, 0, (h->cfg.hidden / 16) * sizeof(int32_t)) != cudaSuccess ||
+        cudaMemset(h->grid_bar, 0, 2 * sizeof(int32_t)) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
   *flags = v;
   return MOE_OK;
 }

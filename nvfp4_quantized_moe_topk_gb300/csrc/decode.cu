@@ -1,0 +1,634 @@
+// decode.cu -- the whole layer in one persistent launch for small batches.
+//
+// At one token the layer reads 6 experts x 5.6 MB of NVFP4 weights and almost
+// nothing else, so its time is set by how early and how fast those bytes
+// stream in.  The Zig/CUDA issue "nvfp4 experts cuda: decode kernels stall on
+// load latency; a cp.async ring makes GLM-5.3 decode up to 24% faster, same
+// bits" (#2265) finds such kernels load-latency bound and fixes them with a
+// per-warp shared-memory ring of weight stages filled ahead of use; gllm pull
+// request #91 ("Results") runs experts with at most 32 tokens on a GEMV.  Here
+// one cooperative kernel (one CTA per SM) does the whole layer:
+//
+//   1. warp 0 routes the <= 1024 pairs in shared memory (counts, offsets,
+//      stable permutation), identically in every CTA;
+//   2. the CTA's share of (expert, 16-row tile) items -- up tiles first, then
+//      down tiles -- is cut into sub-items (a tile's k range split over up to
+//      4 warps when the CTA has few tiles) dealt round-robin to its warps.
+//      Every warp streams its own sub-items: its lane 0 issues 1-D bulk copies
+//      of 4-k-tile weight chunks into the warp's private ring, several chunks
+//      ahead, while the lanes load the matching activation fragments from
+//      global memory one chunk ahead; no warp waits on another in the loop;
+//   3. the warp unpacks its codes exactly to bf16 in registers (bit placement
+//      + one bf16 multiply by the e4m3 scale, see below) and feeds them as A
+//      fragments of warp-level bf16 MMAs with fp32 accumulation; the last warp
+//      to finish a split tile sums the partial tiles in k order and writes it:
+//      relu^2 + bf16 rounding fused into the up store, fp32 rows for down;
+//   4. one grid barrier (a single arrival per CTA) separates up from down; the
+//      weight chunks of the first down tiles are already in flight across it;
+//   5. a per-16-column counter finds the last warp to finish a column block;
+//      that warp applies the WeightedRowSum to those columns of dst for every
+//      token (fixed j order, one fma each, no atomics on data).
+//
+// Fragment-tile weight layout (written once at create): a matrix [G][N][K]
+// becomes tiles [G][N/16][K/64] of 576 bytes -- 512 code bytes, 16 B per lane,
+// then the 16 rows x 4 e4m3 scales.  Within a tile the k order seen by the MMA
+// is permuted so that lane (g = l/4, t = l%4) owns the 16 consecutive k
+// 16t .. 16t+15 of rows g and g+8: that is exactly one scale block per row, and
+// the activation bytes it multiplies are 32 contiguous bytes.  The same
+// permutation is applied to the activations simply by where each lane loads
+// them from, so the MMA sums the right products.  The 8 codes of one 32-bit
+// word are bit-placed so that each bf16 pair of the A fragment is one or two
+// shifts and one mask away: a code lands as sign|exponent(2)|mantissa(1) in the
+// bf16 sign / low exponent / top mantissa bits, i.e. as e2m1 * 2^-126, and one
+// bf16 multiply by (e4m3 scale * 2^118) gives the exact weight * 2^-8, undone
+// by scaling alpha by 2^8.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+// ------------------------------------------------------------------ repack
+// Bit position of code bit `b` (0 mantissa, 1 exponent lsb, 2 exponent msb,
+// 3 sign) of the low (h = 0) or high (h = 1) element of pair slot p (0..3) of
+// a 32-bit word.  Slots 0..2 are the translates of {6,7,8,15 | 22,23,24,31} by
+// 0, -3, -6; slot 3 takes the remaining bits {10,11,13,14 | 26,27,29,30}.
+__host__ __device__ constexpr int code_bit_pos(int p, int h, int b) {
+  return p < 3 ? (b < 3 ? 6 + b : 15) - 3 * p + 16 * h
+               : (b == 0 ? 10 : b == 1 ? 11 : b == 2 ? 13 : 14) + 16 * h;
+}
+
+__global__ void repack_frag_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
+                                   int32_t G, int32_t N, int32_t K, uint8_t* __restrict__ out) {
+  const int32_t KT = K / 64, NT = N / 16;
+  const long long tiles = (long long)G * NT * KT;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < tiles * 32;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long tile = i >> 5;
+    const int lane = (int)(i & 31);
+    const int kt = (int)(tile % KT);
+    const long long rest = tile / KT;
+    const int rt = (int)(rest % NT);
+    const long long grp = rest / NT;
+    const int g = lane >> 2, t = lane & 3;
+    uint32_t words[4];
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const long long row = grp * N + rt * 16 + g + 8 * half;
+      // the lane's 16 codes of this row: k = 64 kt + 16 t .. +15 = 8 code bytes
+      const uint8_t* src = codes + row * (K / 2) + kt * 32 + 8 * t;
+#pragma unroll
+      for (int wq = 0; wq < 2; ++wq) {
+        uint32_t w = 0;
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {  // pair slot p of this word = code byte 4 wq + p
+          const uint32_t byte = src[4 * wq + p];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t code = (byte >> (4 * h)) & 15u;
+#pragma unroll
+            for (int b = 0; b < 4; ++b) w |= ((code >> b) & 1u) << code_bit_pos(p, h, b);
+          }
+        }
+        words[2 * half + wq] = w;
+      }
+    }
+    uint32_t* dst = reinterpret_cast<uint32_t*>(out + tile * kTileBytes + 16 * lane);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) dst[q] = words[q];
+    if (lane < 16) {
+      const long long row = grp * N + rt * 16 + lane;
+      uint8_t* sd = out + tile * kTileBytes + 512 + 4 * lane;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) sd[j] = scales[row * (K / 16) + kt * 4 + j];
+    }
+  }
+}
+
+cudaError_t launch_repack_frag(const uint8_t* codes, const uint8_t* scales, int32_t G, int32_t N, int32_t K,
+                               uint8_t* out, cudaStream_t s) {
+  const long long work = (long long)G * (N / 16) * (K / 64) * 32;
+  long long blocks = (work + 255) / 256;
+  if (blocks > 65535LL * 8) blocks = 65535LL * 8;
+  if (blocks < 1) blocks = 1;
+  repack_frag_kernel<<<(unsigned)blocks, 256, 0, s>>>(codes, scales, G, N, K, out);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ helpers
+// bf16 of (e4m3 byte value) * 2^118, exact (|value| <= 448 keeps it finite).
+__device__ __forceinline__ uint32_t scale_bf16_2p118(uint32_t b) {
+  const uint32_t s = (b >> 7) & 1u, e = (b >> 3) & 15u, m = b & 7u;
+  const float v = (e == 0) ? (float)m * 0x1p109f : __uint_as_float(((e + 238u) << 23) | (m << 20));
+  return (uint32_t)f2bf_rn(v) | (s << 15);
+}
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ float ld_cg_f32(const float* p) {
+  float v;
+  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint4 ld_cg_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ int32_t ld_acquire_gpu(const int32_t* p) {
+  int32_t v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void all_warps_sync(int nthreads) {
+  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+
+// The four bf16 pairs held by one 32-bit word of bit-placed codes, each value
+// e2m1 * 2^-126.
+__device__ __forceinline__ void unpack_word(uint32_t w, uint32_t& p0, uint32_t& p1, uint32_t& p2, uint32_t& p3) {
+  constexpr uint32_t M = 0x81C081C0u;
+  p0 = w & M;
+  p1 = (w << 3) & M;
+  p2 = (w << 6) & M;
+  p3 = ((w >> 4) & 0x00C000C0u) | ((w >> 5) & 0x01000100u) | ((w << 1) & 0x80008000u);
+}
+
+// One chunk (up to kDecCK k-tiles) of one 16-row tile against this lane's
+// activation fragments b (two uint4 = 16 k per k-tile, for token column g).
+__device__ __forceinline__ void chunk_mma(const uint8_t* wts, const uint4 (&b)[kDecCK][2], int kts, int lane,
+                                          const uint32_t* scale_lut, float (&acc)[4], float (&acc2)[4]) {
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int kt = 0; kt < kDecCK; ++kt) {
+    if (kt < kts) {
+      const uint8_t* tile = wts + kt * kTileBytes;
+      const uint4 c = *reinterpret_cast<const uint4*>(tile + 16 * lane);
+      const uint32_t s0 = scale_lut[tile[512 + 4 * g + t]];
+      const uint32_t s1 = scale_lut[tile[512 + 4 * (g + 8) + t]];
+      const uint4 x0 = b[kt][0], x1 = b[kt][1];
+      uint32_t r0, r1, r2, r3;  // row g
+      uint32_t q0, q1, q2, q3;  // row g + 8
+      // word 0 of each row: k blocks 0 and 1 of the MMA
+      unpack_word(c.x, r0, r1, r2, r3);
+      unpack_word(c.z, q0, q1, q2, q3);
+      mma_bf16_16816(acc, mul_bf16x2(r0, s0), mul_bf16x2(q0, s1), mul_bf16x2(r1, s0), mul_bf16x2(q1, s1), x0.x,
+                     x0.y);
+      mma_bf16_16816(acc2, mul_bf16x2(r2, s0), mul_bf16x2(q2, s1), mul_bf16x2(r3, s0), mul_bf16x2(q3, s1), x0.z,
+                     x0.w);
+      // word 1 of each row: k blocks 2 and 3
+      unpack_word(c.y, r0, r1, r2, r3);
+      unpack_word(c.w, q0, q1, q2, q3);
+      mma_bf16_16816(acc, mul_bf16x2(r0, s0), mul_bf16x2(q0, s1), mul_bf16x2(r1, s0), mul_bf16x2(q1, s1), x1.x,
+                     x1.y);
+      mma_bf16_16816(acc2, mul_bf16x2(r2, s0), mul_bf16x2(q2, s1), mul_bf16x2(r3, s0), mul_bf16x2(q3, s1), x1.z,
+                     x1.w);
+    }
+  }
+}
+
+// ------------------------------------------------------------ work cursor
+// One sub-item: k-tiles [kt_lo, kt_hi) of 16-row tile rt of expert e, for
+// every token routed to e (in passes of up to 8), up or down projection.
+struct SubItem {
+  int32_t up, il, ks, e, rt, kt_lo, kt_hi, nch, cnt, off;
+};
+// Position in a warp's chunk sequence: sub-item j, pass at token tok0, chunk.
+struct Cursor {
+  int32_t j, tok0, chunk;
+  SubItem s;
+};
+
+struct DecodeCtx {
+  const DecodeArgs& a;
+  const int32_t* s_tok;     // packed row -> token
+  const int32_t* s_counts;  // [E]
+  const int32_t* s_off;     // [E+1]
+  const int32_t* s_act;     // active experts in expert order
+  int32_t u_lo, d_lo;       // first global up / down item of this CTA
+  int32_t lg_up, lg_dn;     // log2 of the k-split of up / down items
+  int32_t NU, NJ;           // sub-items: up ones, all
+  int32_t W, pass_tok;
+  int32_t KTu, KTd, NTu, NTd;
+
+  __device__ DecodeCtx(const DecodeArgs& args) : a(args) {}
+
+  __device__ __forceinline__ SubItem sub(int32_t j) const {
+    SubItem s;
+    int32_t flat, KT, NT, lg;
+    if (j < NU) {
+      s.up = 1; lg = lg_up; KT = KTu; NT = NTu;
+      s.il = j >> lg; s.ks = j & ((1 << lg) - 1); flat = u_lo + s.il;
+    } else {
+      s.up = 0; lg = lg_dn; KT = KTd; NT = NTd;
+      const int32_t jj = j - NU;
+      s.il = jj >> lg; s.ks = jj & ((1 << lg) - 1); flat = d_lo + s.il;
+    }
+    const int32_t ei = flat / NT;
+    s.rt = flat - ei * NT;
+    s.e = s_act[ei];
+    s.kt_lo = (s.ks * KT) >> lg;
+    s.kt_hi = ((s.ks + 1) * KT) >> lg;
+    s.nch = (s.kt_hi - s.kt_lo + kDecCK - 1) / kDecCK;
+    s.cnt = s_counts[s.e];
+    s.off = s_off[s.e];
+    return s;
+  }
+  __device__ __forceinline__ Cursor start(int32_t j) const {
+    Cursor c;
+    c.j = j; c.tok0 = 0; c.chunk = 0;
+    if (j < NJ) c.s = sub(j);
+    return c;
+  }
+  __device__ __forceinline__ void advance(Cursor& c) const {
+    if (++c.chunk < c.s.nch) return;
+    c.chunk = 0;
+    c.tok0 += pass_tok;
+    if (c.tok0 < c.s.cnt) return;
+    c.tok0 = 0;
+    c.j += W;
+    if (c.j < NJ) c.s = sub(c.j);
+  }
+  __device__ __forceinline__ int32_t kts(const Cursor& c) const {
+    const int32_t kt0 = c.s.kt_lo + c.chunk * kDecCK;
+    return min(kDecCK, c.s.kt_hi - kt0);
+  }
+  // Lane 0 only: bulk-copy the chunk's weight tiles into a ring slot.
+  __device__ __forceinline__ void issue_weights(const Cursor& c, uint8_t* slot, uint64_t* bar,
+                                                uint64_t pol) const {
+    const int32_t KT = c.s.up ? KTu : KTd, NT = c.s.up ? NTu : NTd;
+    const int32_t kt0 = c.s.kt_lo + c.chunk * kDecCK;
+    const uint8_t* base = c.s.up ? a.up_tiles : a.dn_tiles;
+    const uint8_t* src = base + ((size_t)((size_t)c.s.e * NT + c.s.rt) * KT + kt0) * kTileBytes;
+    const uint32_t bytes = (uint32_t)kts(c) * kTileBytes;
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_g2s_hint(slot, src, bytes, bar, pol);
+  }
+  // This lane's activation fragments for the chunk: token column g of the
+  // pass (clamped to the last live token), k = 64 kt + 16 t .. +15.
+  __device__ __forceinline__ void load_acts(const Cursor& c, int lane, uint4 (&b)[kDecCK][2]) const {
+    const int g = lane >> 2, t = lane & 3;
+    const int32_t nt = min(pass_tok, c.s.cnt - c.tok0);
+    const int32_t pr = c.s.off + c.tok0 + min(g, nt - 1);
+    const int32_t kt0 = c.s.kt_lo + c.chunk * kDecCK;
+    const int32_t n_kt = kts(c);
+    if (c.s.up) {
+      const uint16_t* src = a.x + (size_t)s_tok[pr] * a.H + kt0 * 64 + 16 * t;
+#pragma unroll
+      for (int kt = 0; kt < kDecCK; ++kt)
+        if (kt < n_kt) {
+          b[kt][0] = ld_nc_v4(src + kt * 64);
+          b[kt][1] = ld_nc_v4(src + kt * 64 + 8);
+        }
+    } else {
+      const uint16_t* src = a.Ap + (size_t)pr * a.I + kt0 * 64 + 16 * t;
+#pragma unroll
+      for (int kt = 0; kt < kDecCK; ++kt)
+        if (kt < n_kt) {
+          b[kt][0] = ld_cg_v4(src + kt * 64);
+          b[kt][1] = ld_cg_v4(src + kt * 64 + 8);
+        }
+    }
+  }
+};
+
+// ------------------------------------------------------------ kernel
+// Routing of all pairs by warp 0, into shared memory (every CTA computes the
+// same result; CTA 0 also writes it out).  Stable: pairs of one expert keep
+// increasing p order, 32 pairs at a time ranked with a warp match.
+__device__ __forceinline__ void decode_route(const DecodeArgs& a, int lane, const int32_t* s_ids, int32_t* s_tok,
+                                             int32_t* s_inv, const int32_t* s_counts, int32_t* s_off,
+                                             int32_t* s_act, int32_t* misc) {
+  const int32_t E = a.E, R = a.n * a.k;
+  const int32_t per = (E + 31) / 32;
+  const int32_t lo = min(E, lane * per), hi = min(E, lo + per);
+  int32_t sum = 0, nact = 0, cmax = 0;
+  for (int32_t e = lo; e < hi; ++e) {
+    const int32_t c = s_counts[e];
+    sum += c;
+    nact += c > 0;
+    cmax = max(cmax, c);
+  }
+  int32_t isum = sum, iact = nact;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int32_t vs = __shfl_up_sync(0xffffffffu, isum, d);
+    const int32_t va = __shfl_up_sync(0xffffffffu, iact, d);
+    if (lane >= d) { isum += vs; iact += va; }
+  }
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) cmax = max(cmax, __shfl_xor_sync(0xffffffffu, cmax, d));
+  int32_t run = isum - sum, ai = iact - nact;
+  for (int32_t e = lo; e < hi; ++e) {
+    const int32_t c = s_counts[e];
+    s_off[e] = run;
+    run += c;
+    if (c > 0) s_act[ai++] = e;
+  }
+  if (lane == 31) {
+    s_off[E] = isum;
+    misc[1] = iact;
+    misc[2] = cmax;
+  }
+  __syncwarp();
+  const bool cta0 = blockIdx.x == 0;
+  for (int32_t base = 0; base < R; base += 32) {
+    const int32_t p = base + lane;
+    const bool live = p < R;
+    const int32_t e = live ? s_ids[p] : -1;
+    const bool valid = live && e >= 0 && e < E;
+    const uint32_t peers = __match_any_sync(0xffffffffu, valid ? e : -1);
+    const int32_t rank = __popc(peers & ((1u << lane) - 1u));
+    const int32_t pos = valid ? s_off[e] + rank : -1;
+    __syncwarp();
+    if (valid && rank == 0) s_off[e] += __popc(peers);
+    __syncwarp();
+    if (live) {
+      s_inv[p] = pos;
+      if (valid) s_tok[pos] = p / a.k;
+      if (cta0) {
+        a.g_inv[p] = pos;
+        if (valid) a.g_perm[pos] = p;
+      }
+    }
+  }
+  __syncwarp();
+  for (int32_t e = lo; e < hi; ++e) s_off[e] -= s_counts[e];
+  __syncwarp();
+  if (cta0) {
+    for (int32_t e = lane; e < E; e += 32) {
+      a.g_counts[e] = s_counts[e];
+      a.g_offsets[e] = s_off[e];
+    }
+    if (lane == 0) a.g_offsets[E] = s_off[E];
+  }
+}
+
+// One arrival per CTA, then poll until every CTA has arrived (bounded).
+__device__ __forceinline__ void decode_grid_barrier(const DecodeArgs& a, int tid, int nthreads) {
+  all_warps_sync(nthreads);
+  if (tid == 0) {
+    __threadfence();
+    atomicAdd(&a.grid_bar[0], 1);
+    const int32_t want = (int32_t)gridDim.x;
+    if (ld_acquire_gpu(&a.grid_bar[0]) < want) {
+      const uint64_t t0 = globaltimer_ns();
+      while (ld_acquire_gpu(&a.grid_bar[0]) < want) {
+        __nanosleep(32);
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+          atomicOr(a.err, kFlagTimeout);
+          break;
+        }
+      }
+    }
+    __threadfence();
+  }
+  all_warps_sync(nthreads);
+}
+
+__device__ __forceinline__ int32_t choose_split_lg(int32_t items, int32_t KT, int32_t cmax, int32_t W) {
+  int32_t lg = 0;
+  if (cmax <= kDecPassTok)
+    while ((1 << lg) < kDecMaxSplit && (2 << lg) <= KT && items * (2 << lg) <= kDecPartials && (items << lg) < 2 * W)
+      ++lg;
+  return lg;
+}
+
+// A pass of a sub-item is done: reduce split partials (last warp of the tile
+// only), apply alpha, store, and for a finished down tile run the combine of
+// its 16 columns if it was the last tile of them.
+__device__ __forceinline__ void decode_epilogue(const DecodeCtx& cx, const Cursor& cur, float (&v)[4], int lane,
+                                                float4* partial, int32_t* pcount, const int32_t* s_inv,
+                                                int32_t n_act) {
+  const DecodeArgs& a = cx.a;
+  const SubItem& s = cur.s;
+  const int32_t lg = s.up ? cx.lg_up : cx.lg_dn;
+  if (lg > 0) {
+    const int32_t S = 1 << lg;
+    const int32_t base = (s.up ? 0 : kDecPartials) + s.il * S;
+    partial[(base + s.ks) * 32 + lane] = make_float4(v[0], v[1], v[2], v[3]);
+    __threadfence_block();
+    __syncwarp();
+    int32_t last = 0;
+    if (lane == 0) last = atomicAdd(&pcount[(s.up ? 0 : kDecPartials) + s.il], 1) == S - 1;
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (!last) return;
+    __threadfence_block();
+    float4 r = partial[base * 32 + lane];
+    for (int32_t q = 1; q < S; ++q) {
+      const float4 u = partial[(base + q) * 32 + lane];
+      r.x += u.x; r.y += u.y; r.z += u.z; r.w += u.w;
+    }
+    v[0] = r.x; v[1] = r.y; v[2] = r.z; v[3] = r.w;
+  }
+  const int g = lane >> 2, t = lane & 3;
+  const float alpha = (s.up ? a.up_g : a.dn_g)[s.e] * 256.0f;
+  const int32_t nt = min(cx.pass_tok, s.cnt - cur.tok0);
+  const int32_t r0 = s.rt * 16 + g;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int32_t col = 2 * t + (q & 1);
+    const int32_t row = r0 + 8 * (q >> 1);
+    if (col < nt) {
+      const size_t pr = (size_t)(s.off + cur.tok0 + col);
+      const float h = v[q] * alpha;
+      if (s.up) {
+        const float rl = h > 0.0f ? h : 0.0f;
+        a.Ap[pr * a.I + row] = f2bf_rn(rl * rl);
+      } else {
+        a.Yp[pr * a.H + row] = h;
+      }
+    }
+  }
+  if (s.up || cur.tok0 + cx.pass_tok < s.cnt) return;
+  // down tile complete: count it against its 16 columns
+  __threadfence();
+  __syncwarp();
+  int32_t last = 0;
+  if (lane == 0) {
+    last = atomicAdd(&a.col_done[s.rt], 1) == n_act - 1;
+    if (last) a.col_done[s.rt] = 0;
+  }
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (!last) return;
+  __threadfence();
+  const int32_t c = s.rt * 16 + (lane & 15);
+  for (int32_t tk = lane >> 4; tk < a.n; tk += 2) {
+    uint16_t* d = a.dst + (size_t)tk * a.H + c;
+    float acc = __uint_as_float((uint32_t)*d << 16);
+    for (int32_t j = 0; j < a.k; ++j) {
+      const int32_t r = s_inv[tk * a.k + j];
+      if (r >= 0) acc = __fmaf_rn(a.tw[tk * a.k + j], ld_cg_f32(a.Yp + (size_t)r * a.H + c), acc);
+    }
+    *d = f2bf_rn(acc);
+  }
+}
+
+__global__ void __launch_bounds__(kDecMaxWarps * 32, 1) decode_kernel(const __grid_constant__ DecodeArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const DecLayout& L = a.L;
+  uint32_t* lut = reinterpret_cast<uint32_t*>(smem + L.scale_lut);
+  int32_t* s_ids = reinterpret_cast<int32_t*>(smem + L.ids);
+  int32_t* s_tok = reinterpret_cast<int32_t*>(smem + L.perm);
+  int32_t* s_inv = reinterpret_cast<int32_t*>(smem + L.inv);
+  int32_t* s_counts = reinterpret_cast<int32_t*>(smem + L.counts);
+  int32_t* s_off = reinterpret_cast<int32_t*>(smem + L.offsets);
+  int32_t* s_act = reinterpret_cast<int32_t*>(smem + L.act);
+  int32_t* misc = reinterpret_cast<int32_t*>(smem + L.misc);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
+  float4* partial = reinterpret_cast<float4*>(smem + L.partial);
+  int32_t* pcount = reinterpret_cast<int32_t*>(smem + L.pcount);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nthreads = blockDim.x, W = nthreads >> 5;
+  const int32_t R = a.n * a.k, E = a.E;
+
+  for (int i = tid; i < 256; i += nthreads) lut[i] = scale_bf16_2p118((uint32_t)i) * 0x10001u;
+  for (int i = tid; i < 2 * kDecPartials; i += nthreads) pcount[i] = 0;
+  for (int32_t i = tid; i < R; i += nthreads) s_ids[i] = a.ids[i];
+  for (int32_t i = tid; i < E; i += nthreads) s_counts[i] = 0;
+  if (lane == 0) {
+    for (int q = 0; q < kDecMaxSlots; ++q) mbar_init(&bars[warp * kDecMaxSlots + q], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  bool bad = false;
+  for (int32_t p = tid; p < R; p += nthreads) {
+    const int32_t e = s_ids[p];
+    if (e >= 0 && e < E) atomicAdd(&s_counts[e], 1);
+    else bad = true;
+  }
+  if (bad && blockIdx.x == 0) atomicOr(a.err, kFlagBadRouting);
+  __syncthreads();
+  if (warp == 0) decode_route(a, lane, s_ids, s_tok, s_inv, s_counts, s_off, s_act, misc);
+  __syncthreads();
+
+  const int32_t n_act = misc[1], cmax = misc[2];
+  DecodeCtx cx(a);
+  cx.s_tok = s_tok; cx.s_counts = s_counts; cx.s_off = s_off; cx.s_act = s_act;
+  cx.W = W;
+  cx.KTu = a.H / 64; cx.KTd = a.I / 64; cx.NTu = a.I / 16; cx.NTd = a.H / 16;
+  {
+    const int64_t G = gridDim.x, b = blockIdx.x;
+    const int64_t U = (int64_t)n_act * cx.NTu, D = (int64_t)n_act * cx.NTd;
+    cx.u_lo = (int32_t)(U * b / G);
+    cx.d_lo = (int32_t)(D * b / G);
+    const int32_t n_up = (int32_t)(U * (b + 1) / G) - cx.u_lo;
+    const int32_t n_dn = (int32_t)(D * (b + 1) / G) - cx.d_lo;
+    cx.pass_tok = max(1, min(kDecPassTok, cmax));
+    cx.lg_up = choose_split_lg(n_up, cx.KTu, cmax, W);
+    cx.lg_dn = choose_split_lg(n_dn, cx.KTd, cmax, W);
+    cx.NU = n_up << cx.lg_up;
+    cx.NJ = cx.NU + (n_dn << cx.lg_dn);
+  }
+  const int32_t P = min(kDecMaxSlots, (int32_t)((L.total - L.ring) / ((uint32_t)W * kDecSlotBytes)));
+  uint8_t* ring = smem + L.ring + (size_t)warp * P * kDecSlotBytes;
+  uint64_t* wbar = bars + warp * kDecMaxSlots;
+  const uint64_t pol = policy_evict_first();
+
+  // prologue: the first P chunks of this warp's sequence in flight
+  Cursor ci = cx.start(warp);
+  Cursor cc = ci;
+  int32_t issued = 0;
+  for (; issued < P && ci.j < cx.NJ; ++issued) {
+    if (lane == 0) cx.issue_weights(ci, ring + issued * kDecSlotBytes, &wbar[issued], pol);
+    cx.advance(ci);
+  }
+  uint4 bn[kDecCK][2];
+  bool crossed = false, dead = false;
+  if (cc.j < cx.NJ && cc.s.up) cx.load_acts(cc, lane, bn);
+  int32_t consumed = 0, slot = 0;
+  uint32_t phase = 0;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
+  while (cc.j < cx.NJ) {
+    if (!cc.s.up && !crossed) {
+      // every up tile of every CTA is stored before any down tile reads Ap
+      decode_grid_barrier(a, tid, nthreads);
+      crossed = true;
+      cx.load_acts(cc, lane, bn);
+    }
+    const bool ok = mbar_wait_sleep(&wbar[slot], phase, a.err);
+    if (__any_sync(0xffffffffu, !ok)) {
+      dead = true;
+      break;
+    }
+    uint4 bc[kDecCK][2];
+#pragma unroll
+    for (int q = 0; q < kDecCK; ++q) { bc[q][0] = bn[q][0]; bc[q][1] = bn[q][1]; }
+    const Cursor cur = cc;
+    cx.advance(cc);
+    if (cc.j < cx.NJ && (cc.s.up || crossed)) cx.load_acts(cc, lane, bn);
+    chunk_mma(ring + slot * kDecSlotBytes, bc, cx.kts(cur), lane, lut, acc, acc2);
+    ++consumed;
+    __syncwarp();
+    if (ci.j < cx.NJ) {
+      if (lane == 0) {
+        fence_proxy_async_smem();
+        cx.issue_weights(ci, ring + slot * kDecSlotBytes, &wbar[slot], pol);
+      }
+      cx.advance(ci);
+      ++issued;
+    }
+    if (++slot == P) { slot = 0; phase ^= 1u; }
+    if (cur.chunk == cur.s.nch - 1) {
+      float v[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) { v[q] = acc[q] + acc2[q]; acc[q] = 0.f; acc2[q] = 0.f; }
+      decode_epilogue(cx, cur, v, lane, partial, pcount, s_inv, n_act);
+    }
+  }
+  if (!crossed) decode_grid_barrier(a, tid, nthreads);
+  if (dead) {
+    // let this warp's copies still in flight land before the CTA exits
+    for (int32_t c = consumed; c < issued; ++c) mbar_wait_sleep(&wbar[c % P], (uint32_t)((c / P) & 1), a.err);
+  }
+  all_warps_sync(nthreads);
+  if (tid == 0) {
+    __threadfence();
+    if (atomicAdd(&a.grid_bar[1], 1) == (int32_t)gridDim.x - 1) {
+      a.grid_bar[0] = 0;
+      a.grid_bar[1] = 0;
+    }
+  }
+}
+
+DecLayout decode_layout(int32_t E, int32_t R) { return dec_layout(E, R, 227 * 1024 - 1024); }
+
+cudaError_t launch_decode(const DecodeArgs& args, int num_sms, cudaStream_t s) {
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)num_sms);
+  cfg.blockDim = dim3(args.L.warps * 32);
+  cfg.dynamicSmemBytes = args.L.total;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_kernel, args);
+}
+
+}  // namespace moe

@@ -58,6 +58,81 @@ struct GemmArgs {
 cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int num_sms,
                         cudaStream_t s, bool pdl);
 
+// ------------------------------------------------------- decode (small batch)
+// Fragment-tile weight layout and the single-launch small-batch layer (decode.cu).
+constexpr int kTileBytes = 576;        // 16 rows x 64 k: 512 code bytes + 64 scale bytes
+constexpr int kDecMaxWarps = 16;       // warps per CTA
+constexpr int kDecMaxSlots = 8;        // weight-ring slots per warp (at most)
+constexpr int kDecCK = 4;              // k-tiles (of 64) per chunk
+constexpr int kDecSlotBytes = kDecCK * kTileBytes;
+constexpr int kDecPassTok = 8;         // tokens per pass over a tile (one n8 MMA block)
+constexpr int kDecMaxSplit = 4;        // a tile's k range split over up to 4 warps
+constexpr int kDecPartials = 64;       // partial-sum slots per CTA and phase (items x split)
+constexpr int kDecMaxPairs = 1024;
+
+// Shared-memory plan of the decode kernel (byte offsets; the host computes it).
+struct DecLayout {
+  uint32_t scale_lut, ids, perm, inv, counts, offsets, act, misc, bars, partial, pcount, ring, total;
+  uint32_t warps;
+};
+
+inline DecLayout dec_layout(int32_t E, int32_t R, uint32_t budget) {
+  DecLayout L{};
+  uint32_t o = 0;
+  auto take = [&](uint32_t bytes, uint32_t align) {
+    o = (o + align - 1) / align * align;
+    const uint32_t at = o;
+    o += bytes;
+    return at;
+  };
+  L.scale_lut = take(256 * 4, 128);
+  L.ids = take(4 * (uint32_t)R, 16);
+  L.perm = take(4 * (uint32_t)R, 16);
+  L.inv = take(4 * (uint32_t)R, 16);
+  L.counts = take(4 * (uint32_t)E, 16);
+  L.offsets = take(4 * ((uint32_t)E + 1), 16);
+  L.act = take(4 * (uint32_t)E, 16);
+  L.misc = take(64, 16);
+  L.bars = take(8 * kDecMaxSlots * kDecMaxWarps, 16);
+  L.partial = take(2 * kDecPartials * 32 * 16, 128);  // per phase: slots x lanes x float4
+  L.pcount = take(2 * kDecPartials * 4, 16);
+  const uint32_t ring_at = (o + 127) / 128 * 128;
+  uint32_t warps = budget > ring_at ? (budget - ring_at) / (2 * kDecSlotBytes) : 0;
+  if (warps > (uint32_t)kDecMaxWarps) warps = kDecMaxWarps;
+  L.warps = warps;
+  L.ring = ring_at;
+  L.total = budget;
+  return L;
+}
+
+struct DecodeArgs {
+  const uint8_t* up_tiles;    // [E][I/16][H/64][576]
+  const uint8_t* dn_tiles;    // [E][H/16][I/64][576]
+  const float* up_g;
+  const float* dn_g;
+  const uint16_t* x;          // [n][H] bf16
+  const int32_t* ids;         // [n][k]
+  const float* tw;            // [n][k]
+  uint16_t* dst;              // [n][H] bf16
+  uint16_t* Ap;               // [R][I] bf16 (workspace)
+  float* Yp;                  // [R][H] fp32 (workspace)
+  int32_t* g_counts;          // routing results kept for the debug entry point
+  int32_t* g_offsets;
+  int32_t* g_perm;
+  int32_t* g_inv;
+  int32_t* col_done;          // [H/16] combine counters, zero between launches
+  int32_t* grid_bar;          // {arrivals, exits}, zero between launches
+  int32_t* err;
+  int32_t n, H, I, E, k;
+  DecLayout L;
+};
+
+cudaError_t launch_repack_frag(const uint8_t* codes, const uint8_t* scales, int32_t G, int32_t N, int32_t K,
+                               uint8_t* out, cudaStream_t s);
+// Shared-memory plan for E experts and R pairs (227 KB budget).
+DecLayout decode_layout(int32_t E, int32_t R);
+cudaError_t launch_decode(const DecodeArgs& args, int num_sms, cudaStream_t s);
+
 // Host helpers for tensor maps (driver entry point resolved at run time).
 cudaError_t make_tmap_act(CUtensorMap* map, const void* base, uint64_t rows, uint64_t K);
 cudaError_t make_tmap_codes(CUtensorMap* map, const void* base, uint64_t rows, uint64_t K);

@@ -4,7 +4,9 @@ Full-size configs are compared in full where the oracle finishes in seconds
 (tiny, decode-1, decode-32) and on sampled tokens otherwise (each token's
 output depends only on its own row and routing), with the same launch
 configuration the benchmark times.  Intermediates (relu^2 rows, down rows)
-are compared too."""
+are compared too.  Batches with at most 1024 pairs and no expert above the
+GEMV threshold run as the single-launch small-batch kernel; larger ones take
+the multi-kernel path (routing, GEMV, combine), covered by its own cases."""
 import numpy as np
 import pytest
 
@@ -58,8 +60,8 @@ def _check_layer(wl, dev, gemv_max_rows=0, sample=None, check_intermediates=True
             ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(ra), 1e-30))) - 7)
             frac_off = float(np.mean(np.abs(ga - ra) > ulp))
             assert frac_off < 1e-3, f"{frac_off:.2e} of relu^2 values differ by more than one bf16 rounding"
-            okr, e2, r2 = fp_tolerance_check(ga, ra)
-            assert okr, (e2, r2)
+            okr, e2, r2 = layer_tolerance_check(a, ref.a_rows)
+            assert okr, f"relu^2 rows: {e2} vs rms {r2}"
             oky, e3, r3 = fp_tolerance_check(y, ref.y_rows)
             assert oky, f"down rows: {e3} vs rms {r3}"
     else:
@@ -71,7 +73,7 @@ def _check_layer(wl, dev, gemv_max_rows=0, sample=None, check_intermediates=True
     return got
 
 
-def test_tiny_gemv_only(dev):
+def test_tiny_single_launch(dev):
     _check_layer(W.generate("tiny"), dev, gemv_max_rows=1 << 30)
 
 
@@ -89,8 +91,68 @@ def test_decode_32(dev):
 
 @pytest.mark.parametrize("n,H,I,E,k,seed", [(1, 64, 64, 1, 1, 10), (7, 128, 192, 5, 3, 11), (13, 320, 256, 9, 4, 12),
                                              (2, 4096, 2048, 4, 2, 13)])
-def test_small_shapes_gemv(dev, n, H, I, E, k, seed):
+def test_small_shapes_single_launch(dev, n, H, I, E, k, seed):
     _check_layer(W.small_custom(n, H, I, E, k, seed), dev, gemv_max_rows=1 << 30)
+
+
+@pytest.mark.parametrize("n,H,I,E,k,seed", [(40, 64, 64, 32, 32, 34), (300, 128, 192, 5, 4, 35),
+                                             (129, 1024, 512, 16, 8, 36)])
+def test_pairs_above_single_launch_limit_use_general_path(dev, n, H, I, E, k, seed):
+    # more than 1024 pairs: routing kernel, GEMV up / down, combine
+    wl = W.small_custom(n, H, I, E, k, seed)
+    assert wl.R > 1024
+    _check_layer(wl, dev, gemv_max_rows=1 << 30, check_intermediates=wl.R * (H + I) < 1 << 22)
+
+
+def test_decode_duplicates_force_multiple_token_passes(dev):
+    # every pair on one expert: 40 rows of expert 1, five 8-token passes per tile
+    wl = W.small_custom(20, 128, 128, 3, 2, seed=30)
+    wl.topk_ids[:] = 1
+    _check_layer(wl, dev, gemv_max_rows=1 << 30)
+
+
+def test_decode_max_pairs_and_many_experts(dev):
+    wl = W.small_custom(32, 64, 64, 1024, 32, seed=31)
+    assert wl.R == 1024
+    _check_layer(wl, dev, gemv_max_rows=1 << 30, check_intermediates=False)
+
+
+def test_decode_bad_ids_dropped_and_flagged(dev):
+    from nvfp4_quantized_moe_topk_gb300 import api
+
+    wl = W.small_custom(8, 128, 64, 4, 2, seed=32)
+    wl.topk_ids[1] = [7, -1]
+    wl.topk_ids[3, 0] = 4
+    layer = make_layer(wl, dev, gemv_max_rows=1 << 30)
+    got = run_forward(layer, wl, dev)
+    assert layer.device_error() & api.DEVFLAG_BAD_ROUTING
+    ref = oracle.moe_forward(wl)
+    ok, err, rms = layer_tolerance_check(got, ref.dst)
+    assert ok, (err, rms)
+    assert np.array_equal(got[1], wl.dst[1])  # both of token 1's pairs dropped: dst row untouched
+    layer.close()
+
+
+def test_decode_all_ids_invalid_leaves_dst(dev):
+    from nvfp4_quantized_moe_topk_gb300 import api
+
+    wl = W.small_custom(4, 64, 64, 2, 2, seed=33)
+    wl.topk_ids[:] = 2
+    layer = make_layer(wl, dev, gemv_max_rows=1 << 30)
+    got = run_forward(layer, wl, dev)
+    assert np.array_equal(got, wl.dst)
+    assert layer.device_error() & api.DEVFLAG_BAD_ROUTING
+    layer.close()
+
+
+def test_decode_repeated_calls_are_identical(dev):
+    wl = W.generate("decode-1")
+    layer = make_layer(wl, dev)
+    first = run_forward(layer, wl, dev)
+    for _ in range(4):
+        assert np.array_equal(run_forward(layer, wl, dev), first)
+    assert layer.device_error() == 0
+    layer.close()
 
 
 def test_duplicate_expert_ids(dev):
