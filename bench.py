@@ -100,6 +100,10 @@ def algorithmic_work(wl, ids_list, T):
             per["gather"][0] += n * k * H * 2 * 2
     m = len(ids_list)
     out = {kname: (b / m, f / m) for kname, (b, f) in per.items()}
+    if gemm_path:
+        # experts at or below the threshold run in one streaming launch (both projections)
+        out["small_experts"] = (out["gemv_up"][0] + out["gemv_down"][0], out["gemv_up"][1] + out["gemv_down"][1])
+        del out["gemv_up"], out["gemv_down"]
     if decode_single_launch(n, k, T):
         # the whole layer is one kernel: its bytes are those of the four steps it fuses
         parts = ("routing", "gemv_up", "gemv_down", "combine")
@@ -382,7 +386,8 @@ def run_ours(args):
     layer.close()
 
     clocks = clk.summary()
-    launches_per_step = 1 if decode_single_launch(wl.n, wl.k, T) else 4 + (3 if wl.n > T else 0)
+    # single launch; or routing, gather, small experts, 2 GEMMs, combine; or routing, 2 GEMVs, combine
+    launches_per_step = 1 if decode_single_launch(wl.n, wl.k, T) else (6 if wl.n > T else 4)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",

@@ -30,9 +30,11 @@ namespace {
 
 using namespace moe;
 
-enum KernelId { kKRouting = 0, kKGather, kKGemvUp, kKGemmUp, kKGemvDown, kKGemmDown, kKCombine, kKDecode, kKCount };
-const char* const kKernelNames[kKCount] = {"routing",   "gather",    "gemv_up", "gemm_up",
-                                           "gemv_down", "gemm_down", "combine", "decode"};
+enum KernelId {
+  kKRouting = 0, kKGather, kKGemvUp, kKGemmUp, kKGemvDown, kKGemmDown, kKCombine, kKDecode, kKSmall, kKCount
+};
+const char* const kKernelNames[kKCount] = {"routing",   "gather",    "gemv_up", "gemm_up",      "gemv_down",
+                                           "gemm_down", "combine",   "decode",  "small_experts"};
 
 struct TimingSlot {
   cudaEvent_t beg = nullptr, end = nullptr;
@@ -252,33 +254,33 @@ static moe_status forward_impl(moe_nvfp4* h, const uint16_t* x, const int32_t* i
   const bool pdl = !h->timing;
   h->last_n = n;
   cudaError_t e;
+  DecodeArgs d{};
+  d.up_tiles = h->up_tiles;
+  d.dn_tiles = h->dn_tiles;
+  d.up_g = h->up_g;
+  d.dn_g = h->dn_g;
+  d.x = x;
+  d.ids = ids;
+  d.tw = tw;
+  d.dst = dst;
+  d.Ap = h->Ap;
+  d.Yp = h->Yp;
+  d.g_counts = h->counts;
+  d.g_offsets = h->offsets;
+  d.g_perm = h->perm_pair;
+  d.g_inv = h->inv;
+  d.col_done = h->col_done;
+  d.grid_bar = h->grid_bar;
+  d.err = h->err;
+  d.n = n;
+  d.H = H;
+  d.I = I;
+  d.E = E;
+  d.k = k;
   if (!gemm && R <= kDecMaxPairs) {
-    const DecLayout L = decode_layout(E, R);
-    if (L.warps >= 4) {
-      DecodeArgs d{};
-      d.up_tiles = h->up_tiles;
-      d.dn_tiles = h->dn_tiles;
-      d.up_g = h->up_g;
-      d.dn_g = h->dn_g;
-      d.x = x;
-      d.ids = ids;
-      d.tw = tw;
-      d.dst = dst;
-      d.Ap = h->Ap;
-      d.Yp = h->Yp;
-      d.g_counts = h->counts;
-      d.g_offsets = h->offsets;
-      d.g_perm = h->perm_pair;
-      d.g_inv = h->inv;
-      d.col_done = h->col_done;
-      d.grid_bar = h->grid_bar;
-      d.err = h->err;
-      d.n = n;
-      d.H = H;
-      d.I = I;
-      d.E = E;
-      d.k = k;
-      d.L = L;
+    // the whole layer in one launch
+    d.L = decode_layout(E, R);
+    if (d.L.warps >= 4) {
       TimedLaunch tl(h, s, kKDecode);
       return cuda_status(launch_decode(d, h->num_sms, s));
     }
@@ -293,6 +295,21 @@ static moe_status forward_impl(moe_nvfp4* h, const uint16_t* x, const int32_t* i
     e = launch_gather(x, h->perm_pair, h->offsets + E, R, k, H, h->Xp, s, pdl);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
+  // Experts with 0 < rows <= threshold: the same streaming kernel, fed by the
+  // routing kernel's arrays (both projections in one launch); the GEMV pair
+  // below is the fallback when its shared-memory plan does not fit.
+  bool small_done = false;
+  if (gemm) {
+    d.ext = 1;
+    d.max_rows = h->threshold;
+    d.L = decode_layout(E, 0);
+    if (d.L.warps >= 4) {
+      TimedLaunch tl(h, s, kKSmall);
+      e = launch_decode(d, h->num_sms, s);
+      if (e != cudaSuccess) return MOE_ERR_CUDA;
+      small_done = true;
+    }
+  }
   GemvArgs g{};
   g.counts = h->counts;
   g.offsets = h->offsets;
@@ -300,7 +317,7 @@ static moe_status forward_impl(moe_nvfp4* h, const uint16_t* x, const int32_t* i
   g.E = E;
   g.k = k;
   g.max_rows = gemm ? h->threshold : 0;
-  {
+  if (!small_done) {
     TimedLaunch tl(h, s, kKGemvUp);
     g.codes = h->up_codes;
     g.scales = h->up_scales;
@@ -331,7 +348,7 @@ static moe_status forward_impl(moe_nvfp4* h, const uint16_t* x, const int32_t* i
     e = launch_gemm(h->tm_xp, h->tm_up_codes, m, h->num_sms, s, pdl);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
-  {
+  if (!small_done) {
     TimedLaunch tl(h, s, kKGemvDown);
     g.codes = h->dn_codes;
     g.scales = h->dn_scales;

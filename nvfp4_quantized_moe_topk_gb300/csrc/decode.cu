@@ -29,6 +29,12 @@
 //      that warp applies the WeightedRowSum to those columns of dst for every
 //      token (fixed j order, one fma each, no atomics on data).
 //
+// The same kernel also serves the experts with few rows inside a large batch
+// (external-routing mode): it then takes the counts, offsets and permutation
+// that the routing kernel wrote, works only on experts whose row count is at
+// most the GEMV threshold, and leaves the combine to the WeightedRowSum
+// kernel that runs after the grouped GEMMs.
+//
 // Fragment-tile weight layout (written once at create): a matrix [G][N][K]
 // becomes tiles [G][N/16][K/64] of 576 bytes -- 512 code bytes, 16 B per lane,
 // then the 16 rows x 4 e4m3 scales.  Within a tile the k order seen by the MMA
@@ -202,92 +208,119 @@ __device__ __forceinline__ void chunk_mma(const uint8_t* wts, const uint4 (&b)[k
 }
 
 // ------------------------------------------------------------ work cursor
-// One sub-item: k-tiles [kt_lo, kt_hi) of 16-row tile rt of expert e, for
-// every token routed to e (in passes of up to 8), up or down projection.
-struct SubItem {
-  int32_t up, il, ks, e, rt, kt_lo, kt_hi, nch, cnt, off;
+// A warp's work is a sequence of segments: k-tiles [kt, kt_end) of the
+// 16-row tile rt of expert e (local item i of the phase), for tokens tok0 ..
+// tok0 + 7 of that expert.  Phase 0 is the up projection, phase 1 down, 2 done.
+struct Cur {
+  int32_t ph, i, tok0, kt, kt_end, e, rt, cnt, off;
 };
-// Position in a warp's chunk sequence: sub-item j, pass at token tok0, chunk.
-struct Cursor {
-  int32_t j, tok0, chunk;
-  SubItem s;
-};
+
+__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 
 struct DecodeCtx {
   const DecodeArgs& a;
   const int32_t* s_tok;     // packed row -> token
   const int32_t* s_counts;  // [E]
   const int32_t* s_off;     // [E+1]
-  const int32_t* s_act;     // active experts in expert order
-  int32_t u_lo, d_lo;       // first global up / down item of this CTA
-  int32_t lg_up, lg_dn;     // log2 of the k-split of up / down items
-  int32_t NU, NJ;           // sub-items: up ones, all
-  int32_t W, pass_tok;
+  const int32_t* s_act;     // selected experts in expert order
+  const int32_t* g_perm;    // external routing: packed row -> pair
+  int32_t ext;              // 1: routing from global memory, no fused combine
+  int32_t warp, W;
+  int32_t split;            // 1: each phase's k-tiles are cut evenly over the warps (one pass of <= 8 tokens)
+  int32_t u_lo, n_up, d_lo, n_dn;  // this CTA's items per phase
   int32_t KTu, KTd, NTu, NTd;
+  int32_t Wu, Wd;           // warps that take part in each phase (split mode)
+  int32_t ura, urb, dra, drb;      // this warp's tile range per phase (split mode)
 
   __device__ DecodeCtx(const DecodeArgs& args) : a(args) {}
 
-  __device__ __forceinline__ SubItem sub(int32_t j) const {
-    SubItem s;
-    int32_t flat, KT, NT, lg;
-    if (j < NU) {
-      s.up = 1; lg = lg_up; KT = KTu; NT = NTu;
-      s.il = j >> lg; s.ks = j & ((1 << lg) - 1); flat = u_lo + s.il;
-    } else {
-      s.up = 0; lg = lg_dn; KT = KTd; NT = NTd;
-      const int32_t jj = j - NU;
-      s.il = jj >> lg; s.ks = jj & ((1 << lg) - 1); flat = d_lo + s.il;
-    }
+  __device__ __forceinline__ void load_item(Cur& c) const {
+    const int32_t lo = c.ph ? d_lo : u_lo, NT = c.ph ? NTd : NTu;
+    const int32_t flat = lo + c.i;
     const int32_t ei = flat / NT;
-    s.rt = flat - ei * NT;
-    s.e = s_act[ei];
-    s.kt_lo = (s.ks * KT) >> lg;
-    s.kt_hi = ((s.ks + 1) * KT) >> lg;
-    s.nch = (s.kt_hi - s.kt_lo + kDecCK - 1) / kDecCK;
-    s.cnt = s_counts[s.e];
-    s.off = s_off[s.e];
-    return s;
+    c.rt = flat - ei * NT;
+    c.e = s_act[ei];
+    c.cnt = s_counts[c.e];
+    c.off = s_off[c.e];
   }
-  __device__ __forceinline__ Cursor start(int32_t j) const {
-    Cursor c;
-    c.j = j; c.tok0 = 0; c.chunk = 0;
-    if (j < NJ) c.s = sub(j);
-    return c;
+  // First segment of phase ph or a later one (ph = 2 when the warp is done).
+  __device__ __forceinline__ void enter_phase(Cur& c, int32_t ph) const {
+    for (; ph < 2; ++ph) {
+      c.ph = ph;
+      c.tok0 = 0;
+      const int32_t KT = ph ? KTd : KTu;
+      if (split) {
+        const int32_t ra = ph ? dra : ura, rb = ph ? drb : urb;
+        if (ra < rb) {
+          c.i = ra / KT;
+          c.kt = ra - c.i * KT;
+          c.kt_end = min(KT, rb - c.i * KT);
+          load_item(c);
+          return;
+        }
+      } else if (warp < (ph ? n_dn : n_up)) {
+        c.i = warp;
+        c.kt = 0;
+        c.kt_end = KT;
+        load_item(c);
+        return;
+      }
+    }
+    c.ph = 2;
   }
-  __device__ __forceinline__ void advance(Cursor& c) const {
-    if (++c.chunk < c.s.nch) return;
-    c.chunk = 0;
-    c.tok0 += pass_tok;
-    if (c.tok0 < c.s.cnt) return;
-    c.tok0 = 0;
-    c.j += W;
-    if (c.j < NJ) c.s = sub(c.j);
+  __device__ __forceinline__ void advance(Cur& c) const {
+    c.kt += kDecCK;
+    if (c.kt < c.kt_end) return;
+    const int32_t KT = c.ph ? KTd : KTu;
+    if (split) {
+      const int32_t rb = c.ph ? drb : urb;
+      ++c.i;
+      if (c.i * KT < rb) {
+        c.kt = 0;
+        c.kt_end = min(KT, rb - c.i * KT);
+        load_item(c);
+        return;
+      }
+    } else {
+      c.tok0 += kDecPassTok;
+      if (c.tok0 < c.cnt) {
+        c.kt = 0;
+        return;
+      }
+      c.tok0 = 0;
+      c.i += W;
+      if (c.i < (c.ph ? n_dn : n_up)) {
+        c.kt = 0;
+        load_item(c);
+        return;
+      }
+    }
+    enter_phase(c, c.ph + 1);
   }
-  __device__ __forceinline__ int32_t kts(const Cursor& c) const {
-    const int32_t kt0 = c.s.kt_lo + c.chunk * kDecCK;
-    return min(kDecCK, c.s.kt_hi - kt0);
+  __device__ __forceinline__ const uint8_t* chunk_src(const Cur& c) const {
+    const int32_t KT = c.ph ? KTd : KTu, NT = c.ph ? NTd : NTu;
+    const uint8_t* base = c.ph ? a.dn_tiles : a.up_tiles;
+    return base + ((size_t)((size_t)c.e * NT + c.rt) * KT + c.kt) * kTileBytes;
   }
+  __device__ __forceinline__ int32_t kts(const Cur& c) const { return min(kDecCK, c.kt_end - c.kt); }
   // Lane 0 only: bulk-copy the chunk's weight tiles into a ring slot.
-  __device__ __forceinline__ void issue_weights(const Cursor& c, uint8_t* slot, uint64_t* bar,
-                                                uint64_t pol) const {
-    const int32_t KT = c.s.up ? KTu : KTd, NT = c.s.up ? NTu : NTd;
-    const int32_t kt0 = c.s.kt_lo + c.chunk * kDecCK;
-    const uint8_t* base = c.s.up ? a.up_tiles : a.dn_tiles;
-    const uint8_t* src = base + ((size_t)((size_t)c.s.e * NT + c.s.rt) * KT + kt0) * kTileBytes;
+  __device__ __forceinline__ void issue_weights(const Cur& c, uint8_t* slot, uint64_t* bar, uint64_t pol) const {
     const uint32_t bytes = (uint32_t)kts(c) * kTileBytes;
     mbar_arrive_expect_tx(bar, bytes);
-    bulk_g2s_hint(slot, src, bytes, bar, pol);
+    bulk_g2s_hint(slot, chunk_src(c), bytes, bar, pol);
   }
   // This lane's activation fragments for the chunk: token column g of the
   // pass (clamped to the last live token), k = 64 kt + 16 t .. +15.
-  __device__ __forceinline__ void load_acts(const Cursor& c, int lane, uint4 (&b)[kDecCK][2]) const {
+  __device__ __forceinline__ void load_acts(const Cur& c, int lane, uint4 (&b)[kDecCK][2]) const {
     const int g = lane >> 2, t = lane & 3;
-    const int32_t nt = min(pass_tok, c.s.cnt - c.tok0);
-    const int32_t pr = c.s.off + c.tok0 + min(g, nt - 1);
-    const int32_t kt0 = c.s.kt_lo + c.chunk * kDecCK;
+    const int32_t nt = min(kDecPassTok, c.cnt - c.tok0);
+    const int32_t pr = c.off + c.tok0 + min(g, nt - 1);
     const int32_t n_kt = kts(c);
-    if (c.s.up) {
-      const uint16_t* src = a.x + (size_t)s_tok[pr] * a.H + kt0 * 64 + 16 * t;
+    if (c.ph == 0) {
+      const int32_t tok = ext ? __ldg(g_perm + pr) / a.k : s_tok[pr];
+      const uint16_t* src = a.x + (size_t)tok * a.H + c.kt * 64 + 16 * t;
 #pragma unroll
       for (int kt = 0; kt < kDecCK; ++kt)
         if (kt < n_kt) {
@@ -295,7 +328,7 @@ struct DecodeCtx {
           b[kt][1] = ld_nc_v4(src + kt * 64 + 8);
         }
     } else {
-      const uint16_t* src = a.Ap + (size_t)pr * a.I + kt0 * 64 + 16 * t;
+      const uint16_t* src = a.Ap + (size_t)pr * a.I + c.kt * 64 + 16 * t;
 #pragma unroll
       for (int kt = 0; kt < kDecCK; ++kt)
         if (kt < n_kt) {
@@ -378,6 +411,41 @@ __device__ __forceinline__ void decode_route(const DecodeArgs& a, int lane, cons
   }
 }
 
+// External routing: the experts with 0 < count <= max_rows, in expert order,
+// their counts and packed-row offsets as the routing kernel wrote them.
+__device__ __forceinline__ void decode_select(const DecodeArgs& a, int lane, int32_t* s_counts, int32_t* s_off,
+                                              int32_t* s_act, int32_t* misc) {
+  const int32_t E = a.E;
+  const int32_t per = (E + 31) / 32;
+  const int32_t lo = min(E, lane * per), hi = min(E, lo + per);
+  int32_t nact = 0, cmax = 0;
+  for (int32_t e = lo; e < hi; ++e) {
+    const int32_t c = a.g_counts[e];
+    s_counts[e] = c;
+    s_off[e] = a.g_offsets[e];
+    const bool sel = c > 0 && c <= a.max_rows;
+    nact += sel;
+    if (sel) cmax = max(cmax, c);
+  }
+  int32_t iact = nact;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int32_t va = __shfl_up_sync(0xffffffffu, iact, d);
+    if (lane >= d) iact += va;
+  }
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) cmax = max(cmax, __shfl_xor_sync(0xffffffffu, cmax, d));
+  int32_t ai = iact - nact;
+  for (int32_t e = lo; e < hi; ++e) {
+    const int32_t c = s_counts[e];
+    if (c > 0 && c <= a.max_rows) s_act[ai++] = e;
+  }
+  if (lane == 31) {
+    misc[1] = iact;
+    misc[2] = cmax;
+  }
+}
+
 // One arrival per CTA, then poll until every CTA has arrived (bounded).
 __device__ __forceinline__ void decode_grid_barrier(const DecodeArgs& a, int tid, int nthreads) {
   all_warps_sync(nthreads);
@@ -400,53 +468,59 @@ __device__ __forceinline__ void decode_grid_barrier(const DecodeArgs& a, int tid
   all_warps_sync(nthreads);
 }
 
-__device__ __forceinline__ int32_t choose_split_lg(int32_t items, int32_t KT, int32_t cmax, int32_t W) {
-  int32_t lg = 0;
-  if (cmax <= kDecPassTok)
-    while ((1 << lg) < kDecMaxSplit && (2 << lg) <= KT && items * (2 << lg) <= kDecPartials && (items << lg) < 2 * W)
-      ++lg;
-  return lg;
-}
-
-// A pass of a sub-item is done: reduce split partials (last warp of the tile
-// only), apply alpha, store, and for a finished down tile run the combine of
-// its 16 columns if it was the last tile of them.
-__device__ __forceinline__ void decode_epilogue(const DecodeCtx& cx, const Cursor& cur, float (&v)[4], int lane,
+// The segment in `cur` is finished: if the warp holds only part of the tile's
+// k range, park the partial tile and let the last of the tile's warps sum all
+// parts in warp order; then apply alpha and store, and for a finished down
+// tile run the combine of its 16 columns if it was the last tile of them.
+__device__ __forceinline__ void decode_epilogue(const DecodeCtx& cx, const Cur& cur, float (&v)[4], int lane,
                                                 float4* partial, int32_t* pcount, const int32_t* s_inv,
                                                 int32_t n_act) {
   const DecodeArgs& a = cx.a;
-  const SubItem& s = cur.s;
-  const int32_t lg = s.up ? cx.lg_up : cx.lg_dn;
-  if (lg > 0) {
-    const int32_t S = 1 << lg;
-    const int32_t base = (s.up ? 0 : kDecPartials) + s.il * S;
-    partial[(base + s.ks) * 32 + lane] = make_float4(v[0], v[1], v[2], v[3]);
-    __threadfence_block();
-    __syncwarp();
-    int32_t last = 0;
-    if (lane == 0) last = atomicAdd(&pcount[(s.up ? 0 : kDecPartials) + s.il], 1) == S - 1;
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (!last) return;
-    __threadfence_block();
-    float4 r = partial[base * 32 + lane];
-    for (int32_t q = 1; q < S; ++q) {
-      const float4 u = partial[(base + q) * 32 + lane];
-      r.x += u.x; r.y += u.y; r.z += u.z; r.w += u.w;
+  const int32_t up = cur.ph == 0;
+  if (cx.split) {
+    const int32_t KT = up ? cx.KTu : cx.KTd;
+    const int32_t ra = up ? cx.ura : cx.dra;
+    const int32_t first_item = ra / KT;
+    const int32_t seg_lo = cur.i == first_item ? ra - cur.i * KT : 0;
+    if (seg_lo != 0 || cur.kt_end != KT) {
+      const int64_t TT = (int64_t)(up ? cx.n_up : cx.n_dn) * KT;
+      const int64_t Wp = up ? cx.Wu : cx.Wd;
+      const int32_t side = cur.i == first_item ? 0 : 1;
+      partial[(cx.warp * 2 + side) * 32 + lane] = make_float4(v[0], v[1], v[2], v[3]);
+      __threadfence_block();
+      __syncwarp();
+      // warps holding tile rows i*KT .. (i+1)*KT-1 of this phase
+      const int32_t wf = (int32_t)((((int64_t)cur.i * KT + 1) * Wp - 1) / TT);
+      const int32_t wl = (int32_t)((((int64_t)(cur.i + 1) * KT) * Wp - 1) / TT);
+      int32_t last = 0;
+      if (lane == 0) {
+        last = atomicAdd(&pcount[wf], 1) == wl - wf;
+        if (last) pcount[wf] = 0;
+      }
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (!last) return;
+      __threadfence_block();
+      float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int32_t w2 = wf; w2 <= wl; ++w2) {
+        const int32_t fi = (int32_t)((TT * w2) / Wp) / KT;
+        const float4 u = partial[(w2 * 2 + (cur.i == fi ? 0 : 1)) * 32 + lane];
+        r.x += u.x; r.y += u.y; r.z += u.z; r.w += u.w;
+      }
+      v[0] = r.x; v[1] = r.y; v[2] = r.z; v[3] = r.w;
     }
-    v[0] = r.x; v[1] = r.y; v[2] = r.z; v[3] = r.w;
   }
   const int g = lane >> 2, t = lane & 3;
-  const float alpha = (s.up ? a.up_g : a.dn_g)[s.e] * 256.0f;
-  const int32_t nt = min(cx.pass_tok, s.cnt - cur.tok0);
-  const int32_t r0 = s.rt * 16 + g;
+  const float alpha = (up ? a.up_g : a.dn_g)[cur.e] * 256.0f;
+  const int32_t nt = min(kDecPassTok, cur.cnt - cur.tok0);
+  const int32_t r0 = cur.rt * 16 + g;
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const int32_t col = 2 * t + (q & 1);
     const int32_t row = r0 + 8 * (q >> 1);
     if (col < nt) {
-      const size_t pr = (size_t)(s.off + cur.tok0 + col);
+      const size_t pr = (size_t)(cur.off + cur.tok0 + col);
       const float h = v[q] * alpha;
-      if (s.up) {
+      if (up) {
         const float rl = h > 0.0f ? h : 0.0f;
         a.Ap[pr * a.I + row] = f2bf_rn(rl * rl);
       } else {
@@ -454,19 +528,19 @@ __device__ __forceinline__ void decode_epilogue(const DecodeCtx& cx, const Curso
       }
     }
   }
-  if (s.up || cur.tok0 + cx.pass_tok < s.cnt) return;
+  if (up || cx.ext || cur.tok0 + kDecPassTok < cur.cnt) return;
   // down tile complete: count it against its 16 columns
   __threadfence();
   __syncwarp();
   int32_t last = 0;
   if (lane == 0) {
-    last = atomicAdd(&a.col_done[s.rt], 1) == n_act - 1;
-    if (last) a.col_done[s.rt] = 0;
+    last = atomicAdd(&a.col_done[cur.rt], 1) == n_act - 1;
+    if (last) a.col_done[cur.rt] = 0;
   }
   last = __shfl_sync(0xffffffffu, last, 0);
   if (!last) return;
   __threadfence();
-  const int32_t c = s.rt * 16 + (lane & 15);
+  const int32_t c = cur.rt * 16 + (lane & 15);
   for (int32_t tk = lane >> 4; tk < a.n; tk += 2) {
     uint16_t* d = a.dst + (size_t)tk * a.H + c;
     float acc = __uint_as_float((uint32_t)*d << 16);
@@ -498,84 +572,102 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) decode_kernel(const __gr
   const int32_t R = a.n * a.k, E = a.E;
 
   for (int i = tid; i < 256; i += nthreads) lut[i] = scale_bf16_2p118((uint32_t)i) * 0x10001u;
-  for (int i = tid; i < 2 * kDecPartials; i += nthreads) pcount[i] = 0;
-  for (int32_t i = tid; i < R; i += nthreads) s_ids[i] = a.ids[i];
-  for (int32_t i = tid; i < E; i += nthreads) s_counts[i] = 0;
+  for (int i = tid; i < kDecMaxWarps; i += nthreads) pcount[i] = 0;
+  if (!a.ext) {
+    for (int32_t i = tid; i < R; i += nthreads) s_ids[i] = a.ids[i];
+    for (int32_t i = tid; i < E; i += nthreads) s_counts[i] = 0;
+  }
   if (lane == 0) {
     for (int q = 0; q < kDecMaxSlots; ++q) mbar_init(&bars[warp * kDecMaxSlots + q], 1);
     fence_mbar_init();
   }
   __syncthreads();
-  bool bad = false;
-  for (int32_t p = tid; p < R; p += nthreads) {
-    const int32_t e = s_ids[p];
-    if (e >= 0 && e < E) atomicAdd(&s_counts[e], 1);
-    else bad = true;
+  if (a.ext) {
+    if (warp == 0) decode_select(a, lane, s_counts, s_off, s_act, misc);
+  } else {
+    bool bad = false;
+    for (int32_t p = tid; p < R; p += nthreads) {
+      const int32_t e = s_ids[p];
+      if (e >= 0 && e < E) atomicAdd(&s_counts[e], 1);
+      else bad = true;
+    }
+    if (bad && blockIdx.x == 0) atomicOr(a.err, kFlagBadRouting);
+    __syncthreads();
+    if (warp == 0) decode_route(a, lane, s_ids, s_tok, s_inv, s_counts, s_off, s_act, misc);
   }
-  if (bad && blockIdx.x == 0) atomicOr(a.err, kFlagBadRouting);
-  __syncthreads();
-  if (warp == 0) decode_route(a, lane, s_ids, s_tok, s_inv, s_counts, s_off, s_act, misc);
   __syncthreads();
 
   const int32_t n_act = misc[1], cmax = misc[2];
   DecodeCtx cx(a);
   cx.s_tok = s_tok; cx.s_counts = s_counts; cx.s_off = s_off; cx.s_act = s_act;
-  cx.W = W;
+  cx.g_perm = a.g_perm; cx.ext = a.ext;
+  cx.warp = warp; cx.W = W;
   cx.KTu = a.H / 64; cx.KTd = a.I / 64; cx.NTu = a.I / 16; cx.NTd = a.H / 16;
   {
     const int64_t G = gridDim.x, b = blockIdx.x;
     const int64_t U = (int64_t)n_act * cx.NTu, D = (int64_t)n_act * cx.NTd;
     cx.u_lo = (int32_t)(U * b / G);
     cx.d_lo = (int32_t)(D * b / G);
-    const int32_t n_up = (int32_t)(U * (b + 1) / G) - cx.u_lo;
-    const int32_t n_dn = (int32_t)(D * (b + 1) / G) - cx.d_lo;
-    cx.pass_tok = max(1, min(kDecPassTok, cmax));
-    cx.lg_up = choose_split_lg(n_up, cx.KTu, cmax, W);
-    cx.lg_dn = choose_split_lg(n_dn, cx.KTd, cmax, W);
-    cx.NU = n_up << cx.lg_up;
-    cx.NJ = cx.NU + (n_dn << cx.lg_dn);
+    cx.n_up = (int32_t)(U * (b + 1) / G) - cx.u_lo;
+    cx.n_dn = (int32_t)(D * (b + 1) / G) - cx.d_lo;
+    cx.split = cmax <= kDecPassTok;
+    const int64_t TTu = (int64_t)cx.n_up * cx.KTu, TTd = (int64_t)cx.n_dn * cx.KTd;
+    cx.Wu = (int32_t)(TTu < W ? TTu : W);
+    cx.Wd = (int32_t)(TTd < W ? TTd : W);
+    cx.ura = warp < cx.Wu ? (int32_t)(TTu * warp / cx.Wu) : 0;
+    cx.urb = warp < cx.Wu ? (int32_t)(TTu * (warp + 1) / cx.Wu) : 0;
+    cx.dra = warp < cx.Wd ? (int32_t)(TTd * warp / cx.Wd) : 0;
+    cx.drb = warp < cx.Wd ? (int32_t)(TTd * (warp + 1) / cx.Wd) : 0;
   }
   const int32_t P = min(kDecMaxSlots, (int32_t)((L.total - L.ring) / ((uint32_t)W * kDecSlotBytes)));
   uint8_t* ring = smem + L.ring + (size_t)warp * P * kDecSlotBytes;
   uint64_t* wbar = bars + warp * kDecMaxSlots;
   const uint64_t pol = policy_evict_first();
 
-  // prologue: the first P chunks of this warp's sequence in flight
-  Cursor ci = cx.start(warp);
-  Cursor cc = ci;
+  // prologue: the first P chunks of this warp's sequence in flight, the next
+  // kDecL2Ahead chunks requested into L2
+  Cur ci;
+  cx.enter_phase(ci, 0);
+  Cur cc = ci;
   int32_t issued = 0;
-  for (; issued < P && ci.j < cx.NJ; ++issued) {
+  for (; issued < P && ci.ph < 2; ++issued) {
     if (lane == 0) cx.issue_weights(ci, ring + issued * kDecSlotBytes, &wbar[issued], pol);
     cx.advance(ci);
   }
-  uint4 bn[kDecCK][2];
+  {
+    Cur cp = ci;
+    for (int q = 0; q < kDecL2Ahead && cp.ph < 2; ++q) {
+      if (lane == 0) prefetch_l2_bulk(cx.chunk_src(cp), (uint32_t)cx.kts(cp) * kTileBytes);
+      cx.advance(cp);
+    }
+  }
+  uint4 bA[kDecCK][2], bB[kDecCK][2];
   bool crossed = false, dead = false;
-  if (cc.j < cx.NJ && cc.s.up) cx.load_acts(cc, lane, bn);
+  if (cc.ph == 0) cx.load_acts(cc, lane, bA);
   int32_t consumed = 0, slot = 0;
   uint32_t phase = 0;
   float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
-  while (cc.j < cx.NJ) {
-    if (!cc.s.up && !crossed) {
+
+  // One chunk: bc holds its activation fragments, bn receives the next chunk's.
+  auto step = [&](uint4 (&bc)[kDecCK][2], uint4 (&bn)[kDecCK][2]) -> bool {
+    if (cc.ph == 1 && !crossed) {
       // every up tile of every CTA is stored before any down tile reads Ap
       decode_grid_barrier(a, tid, nthreads);
       crossed = true;
-      cx.load_acts(cc, lane, bn);
+      cx.load_acts(cc, lane, bc);
     }
     const bool ok = mbar_wait_sleep(&wbar[slot], phase, a.err);
     if (__any_sync(0xffffffffu, !ok)) {
       dead = true;
-      break;
+      return false;
     }
-    uint4 bc[kDecCK][2];
-#pragma unroll
-    for (int q = 0; q < kDecCK; ++q) { bc[q][0] = bn[q][0]; bc[q][1] = bn[q][1]; }
-    const Cursor cur = cc;
+    const Cur cur = cc;
     cx.advance(cc);
-    if (cc.j < cx.NJ && (cc.s.up || crossed)) cx.load_acts(cc, lane, bn);
+    if (cc.ph == 0 || (cc.ph == 1 && crossed)) cx.load_acts(cc, lane, bn);
     chunk_mma(ring + slot * kDecSlotBytes, bc, cx.kts(cur), lane, lut, acc, acc2);
     ++consumed;
     __syncwarp();
-    if (ci.j < cx.NJ) {
+    if (ci.ph < 2) {
       if (lane == 0) {
         fence_proxy_async_smem();
         cx.issue_weights(ci, ring + slot * kDecSlotBytes, &wbar[slot], pol);
@@ -583,13 +675,25 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) decode_kernel(const __gr
       cx.advance(ci);
       ++issued;
     }
-    if (++slot == P) { slot = 0; phase ^= 1u; }
-    if (cur.chunk == cur.s.nch - 1) {
+    if (++slot == P) {
+      slot = 0;
+      phase ^= 1u;
+    }
+    if (cur.kt + kDecCK >= cur.kt_end) {
       float v[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) { v[q] = acc[q] + acc2[q]; acc[q] = 0.f; acc2[q] = 0.f; }
+      for (int q = 0; q < 4; ++q) {
+        v[q] = acc[q] + acc2[q];
+        acc[q] = 0.f;
+        acc2[q] = 0.f;
+      }
       decode_epilogue(cx, cur, v, lane, partial, pcount, s_inv, n_act);
     }
+    return true;
+  };
+  while (cc.ph < 2) {
+    if (!step(bA, bB) || cc.ph >= 2) break;
+    if (!step(bB, bA)) break;
   }
   if (!crossed) decode_grid_barrier(a, tid, nthreads);
   if (dead) {

@@ -66,8 +66,7 @@ constexpr int kDecMaxSlots = 8;        // weight-ring slots per warp (at most)
 constexpr int kDecCK = 4;              // k-tiles (of 64) per chunk
 constexpr int kDecSlotBytes = kDecCK * kTileBytes;
 constexpr int kDecPassTok = 8;         // tokens per pass over a tile (one n8 MMA block)
-constexpr int kDecMaxSplit = 4;        // a tile's k range split over up to 4 warps
-constexpr int kDecPartials = 64;       // partial-sum slots per CTA and phase (items x split)
+constexpr int kDecL2Ahead = 8;         // chunks past the ring requested into L2 at start
 constexpr int kDecMaxPairs = 1024;
 
 // Shared-memory plan of the decode kernel (byte offsets; the host computes it).
@@ -94,8 +93,8 @@ inline DecLayout dec_layout(int32_t E, int32_t R, uint32_t budget) {
   L.act = take(4 * (uint32_t)E, 16);
   L.misc = take(64, 16);
   L.bars = take(8 * kDecMaxSlots * kDecMaxWarps, 16);
-  L.partial = take(2 * kDecPartials * 32 * 16, 128);  // per phase: slots x lanes x float4
-  L.pcount = take(2 * kDecPartials * 4, 16);
+  L.partial = take(2 * kDecMaxWarps * 32 * 16, 128);  // (warp, first/last segment) x lanes x float4
+  L.pcount = take(kDecMaxWarps * 4, 16);
   const uint32_t ring_at = (o + 127) / 128 * 128;
   uint32_t warps = budget > ring_at ? (budget - ring_at) / (2 * kDecSlotBytes) : 0;
   if (warps > (uint32_t)kDecMaxWarps) warps = kDecMaxWarps;
@@ -124,6 +123,10 @@ struct DecodeArgs {
   int32_t* grid_bar;          // {arrivals, exits}, zero between launches
   int32_t* err;
   int32_t n, H, I, E, k;
+  // ext = 1: routing comes from g_counts / g_offsets / g_perm (written by the
+  // routing kernel), only experts with 0 < count <= max_rows are processed,
+  // and the combine is left to the WeightedRowSum kernel.
+  int32_t ext, max_rows;
   DecLayout L;
 };
 
