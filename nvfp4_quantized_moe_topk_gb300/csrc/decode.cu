@@ -174,50 +174,30 @@ __device__ __forceinline__ void unpack_word(uint32_t w, uint32_t& p0, uint32_t& 
   p3 = ((w >> 4) & 0x00C000C0u) | ((w >> 5) & 0x01000100u) | ((w << 1) & 0x80008000u);
 }
 
-// One chunk (up to kDecCK k-tiles) of one 16-row tile against this lane's
-// activation fragments b (two uint4 = 16 k per k-tile, for token column g).
-__device__ __forceinline__ void chunk_mma(const uint8_t* wts, const uint4 (&b)[kDecCK][2], int kts, int lane,
-                                          const uint32_t* scale_lut, float (&acc)[4], float (&acc2)[4]) {
-  const int g = lane >> 2, t = lane & 3;
-#pragma unroll
-  for (int kt = 0; kt < kDecCK; ++kt) {
-    if (kt < kts) {
-      const uint8_t* tile = wts + kt * kTileBytes;
-      const uint4 c = *reinterpret_cast<const uint4*>(tile + 16 * lane);
-      const uint32_t s0 = scale_lut[tile[512 + 4 * g + t]];
-      const uint32_t s1 = scale_lut[tile[512 + 4 * (g + 8) + t]];
-      const uint4 x0 = b[kt][0], x1 = b[kt][1];
-      uint32_t r0, r1, r2, r3;  // row g
-      uint32_t q0, q1, q2, q3;  // row g + 8
-      // word 0 of each row: k blocks 0 and 1 of the MMA
-      unpack_word(c.x, r0, r1, r2, r3);
-      unpack_word(c.z, q0, q1, q2, q3);
-      mma_bf16_16816(acc, mul_bf16x2(r0, s0), mul_bf16x2(q0, s1), mul_bf16x2(r1, s0), mul_bf16x2(q1, s1), x0.x,
-                     x0.y);
-      mma_bf16_16816(acc2, mul_bf16x2(r2, s0), mul_bf16x2(q2, s1), mul_bf16x2(r3, s0), mul_bf16x2(q3, s1), x0.z,
-                     x0.w);
-      // word 1 of each row: k blocks 2 and 3
-      unpack_word(c.y, r0, r1, r2, r3);
-      unpack_word(c.w, q0, q1, q2, q3);
-      mma_bf16_16816(acc, mul_bf16x2(r0, s0), mul_bf16x2(q0, s1), mul_bf16x2(r1, s0), mul_bf16x2(q1, s1), x1.x,
-                     x1.y);
-      mma_bf16_16816(acc2, mul_bf16x2(r2, s0), mul_bf16x2(q2, s1), mul_bf16x2(r3, s0), mul_bf16x2(q3, s1), x1.z,
-                     x1.w);
-    }
-  }
-}
-
 // ------------------------------------------------------------ work cursor
 // A warp's work is a sequence of segments: k-tiles [kt, kt_end) of the
 // 16-row tile rt of expert e (local item i of the phase), for tokens tok0 ..
 // tok0 + 7 of that expert.  Phase 0 is the up projection, phase 1 down, 2 done.
-struct Cur {
-  int32_t ph, i, tok0, kt, kt_end, e, rt, cnt, off;
+struct __align__(16) Cur {
+  int32_t ph, i, tok0, kt, kt_end, e, rt, cnt, off, pad0, pad1, pad2;
 };
 
 __device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+// The barrier receives one arrival once all of this thread's earlier cp.async
+// copies have landed (counted in the barrier's expected arrivals).
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Ring slot layout: kDecCK weight tiles, then the chunk's activation rows:
+// per token column g < nt, kDecCK x 64 bf16 (128 B per k-tile), rows padded to
+// kDecActRow bytes so the 8 columns of a fragment load hit distinct banks.
+constexpr uint32_t kDecActRow = kDecCK * 128 + 16;
 
 struct DecodeCtx {
   const DecodeArgs& a;
@@ -225,8 +205,6 @@ struct DecodeCtx {
   const int32_t* s_counts;  // [E]
   const int32_t* s_off;     // [E+1]
   const int32_t* s_act;     // selected experts in expert order
-  const int32_t* g_perm;    // external routing: packed row -> pair
-  int32_t ext;              // 1: routing from global memory, no fused combine
   int32_t warp, W;
   int32_t split;            // 1: each phase's k-tiles are cut evenly over the warps (one pass of <= 8 tokens)
   int32_t u_lo, n_up, d_lo, n_dn;  // this CTA's items per phase
@@ -251,6 +229,7 @@ struct DecodeCtx {
       c.ph = ph;
       c.tok0 = 0;
       const int32_t KT = ph ? KTd : KTu;
+      if (warp >= W) continue;
       if (split) {
         const int32_t ra = ph ? dra : ura, rb = ph ? drb : urb;
         if (ra < rb) {
@@ -305,39 +284,72 @@ struct DecodeCtx {
     return base + ((size_t)((size_t)c.e * NT + c.rt) * KT + c.kt) * kTileBytes;
   }
   __device__ __forceinline__ int32_t kts(const Cur& c) const { return min(kDecCK, c.kt_end - c.kt); }
-  // Lane 0 only: bulk-copy the chunk's weight tiles into a ring slot.
+  // Lane 0 only: bulk-copy the chunk's weight tiles into its ring slot.
   __device__ __forceinline__ void issue_weights(const Cur& c, uint8_t* slot, uint64_t* bar, uint64_t pol) const {
     const uint32_t bytes = (uint32_t)kts(c) * kTileBytes;
     mbar_arrive_expect_tx(bar, bytes);
     bulk_g2s_hint(slot, chunk_src(c), bytes, bar, pol);
   }
-  // This lane's activation fragments for the chunk: token column g of the
-  // pass (clamped to the last live token), k = 64 kt + 16 t .. +15.
-  __device__ __forceinline__ void load_acts(const Cur& c, int lane, uint4 (&b)[kDecCK][2]) const {
+  // All lanes: copy the chunk's activation rows (16 B per lane and copy) into
+  // the slot, then arrive on its barrier when they have landed.
+  __device__ __forceinline__ void issue_acts(const Cur& c, int lane, uint8_t* slot, uint64_t* bar) const {
     const int g = lane >> 2, t = lane & 3;
     const int32_t nt = min(kDecPassTok, c.cnt - c.tok0);
-    const int32_t pr = c.off + c.tok0 + min(g, nt - 1);
-    const int32_t n_kt = kts(c);
-    if (c.ph == 0) {
-      const int32_t tok = ext ? __ldg(g_perm + pr) / a.k : s_tok[pr];
-      const uint16_t* src = a.x + (size_t)tok * a.H + c.kt * 64 + 16 * t;
+    if (g < nt) {
+      const int32_t pr = c.off + c.tok0 + g;
+      const uint16_t* src;
+      if (c.ph == 0) {
+        const int32_t tok = a.ext ? __ldg(a.g_perm + pr) / a.k : s_tok[pr];
+        src = a.x + (size_t)tok * a.H + c.kt * 64 + 16 * t;
+      } else {
+        src = a.Ap + (size_t)pr * a.I + c.kt * 64 + 16 * t;
+      }
+      uint8_t* dst = slot + kDecCK * kTileBytes + g * kDecActRow + t * 32;
+      const int32_t n_kt = kts(c);
 #pragma unroll
       for (int kt = 0; kt < kDecCK; ++kt)
         if (kt < n_kt) {
-          b[kt][0] = ld_nc_v4(src + kt * 64);
-          b[kt][1] = ld_nc_v4(src + kt * 64 + 8);
-        }
-    } else {
-      const uint16_t* src = a.Ap + (size_t)pr * a.I + c.kt * 64 + 16 * t;
-#pragma unroll
-      for (int kt = 0; kt < kDecCK; ++kt)
-        if (kt < n_kt) {
-          b[kt][0] = ld_cg_v4(src + kt * 64);
-          b[kt][1] = ld_cg_v4(src + kt * 64 + 8);
+          cp_async16(dst + kt * 128, src + kt * 64);
+          cp_async16(dst + kt * 128 + 16, src + kt * 64 + 8);
         }
     }
+    cp_async_arrive(bar);
   }
 };
+
+// One chunk (up to kDecCK k-tiles of one 16-row tile) against the activation
+// rows staged in the same slot; `act` points at this lane's token column.
+__device__ __forceinline__ void chunk_mma(const uint8_t* wts, const uint8_t* act, int kts, int lane,
+                                          const uint32_t* scale_lut, float (&acc)[4], float (&acc2)[4]) {
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int kt = 0; kt < kDecCK; ++kt) {
+    if (kt < kts) {
+      const uint8_t* tile = wts + kt * kTileBytes;
+      const uint4 c = *reinterpret_cast<const uint4*>(tile + 16 * lane);
+      const uint32_t s0 = scale_lut[tile[512 + 4 * g + t]];
+      const uint32_t s1 = scale_lut[tile[512 + 4 * (g + 8) + t]];
+      const uint4 x0 = *reinterpret_cast<const uint4*>(act + kt * 128);
+      const uint4 x1 = *reinterpret_cast<const uint4*>(act + kt * 128 + 16);
+      uint32_t r0, r1, r2, r3;  // row g
+      uint32_t q0, q1, q2, q3;  // row g + 8
+      // word 0 of each row: k blocks 0 and 1 of the MMA
+      unpack_word(c.x, r0, r1, r2, r3);
+      unpack_word(c.z, q0, q1, q2, q3);
+      mma_bf16_16816(acc, mul_bf16x2(r0, s0), mul_bf16x2(q0, s1), mul_bf16x2(r1, s0), mul_bf16x2(q1, s1), x0.x,
+                     x0.y);
+      mma_bf16_16816(acc2, mul_bf16x2(r2, s0), mul_bf16x2(q2, s1), mul_bf16x2(r3, s0), mul_bf16x2(q3, s1), x0.z,
+                     x0.w);
+      // word 1 of each row: k blocks 2 and 3
+      unpack_word(c.y, r0, r1, r2, r3);
+      unpack_word(c.w, q0, q1, q2, q3);
+      mma_bf16_16816(acc, mul_bf16x2(r0, s0), mul_bf16x2(q0, s1), mul_bf16x2(r1, s0), mul_bf16x2(q1, s1), x1.x,
+                     x1.y);
+      mma_bf16_16816(acc2, mul_bf16x2(r2, s0), mul_bf16x2(q2, s1), mul_bf16x2(r3, s0), mul_bf16x2(q3, s1), x1.z,
+                     x1.w);
+    }
+  }
+}
 
 // ------------------------------------------------------------ kernel
 // Routing of all pairs by warp 0, into shared memory (every CTA computes the
@@ -446,13 +458,13 @@ __device__ __forceinline__ void decode_select(const DecodeArgs& a, int lane, int
   }
 }
 
-// One arrival per CTA, then poll until every CTA has arrived (bounded).
-__device__ __forceinline__ void decode_grid_barrier(const DecodeArgs& a, int tid, int nthreads) {
+// One arrival per CTA, then poll until the arrival count reaches `want`
+// (gridDim.x for the first barrier of a launch, 2 * gridDim.x for the second).
+__device__ __forceinline__ void decode_grid_barrier(const DecodeArgs& a, int tid, int nthreads, int32_t want) {
   all_warps_sync(nthreads);
   if (tid == 0) {
     __threadfence();
     atomicAdd(&a.grid_bar[0], 1);
-    const int32_t want = (int32_t)gridDim.x;
     if (ld_acquire_gpu(&a.grid_bar[0]) < want) {
       const uint64_t t0 = globaltimer_ns();
       while (ld_acquire_gpu(&a.grid_bar[0]) < want) {
@@ -471,7 +483,9 @@ __device__ __forceinline__ void decode_grid_barrier(const DecodeArgs& a, int tid
 // The segment in `cur` is finished: if the warp holds only part of the tile's
 // k range, park the partial tile and let the last of the tile's warps sum all
 // parts in warp order; then apply alpha and store, and for a finished down
-// tile run the combine of its 16 columns if it was the last tile of them.
+// tile run the combine of its 16 columns if it was the last tile of them (for
+// batches of at most kDecLateCombine tokens; larger ones combine after a
+// second grid barrier).
 __device__ __forceinline__ void decode_epilogue(const DecodeCtx& cx, const Cur& cur, float (&v)[4], int lane,
                                                 float4* partial, int32_t* pcount, const int32_t* s_inv,
                                                 int32_t n_act) {
@@ -528,7 +542,7 @@ __device__ __forceinline__ void decode_epilogue(const DecodeCtx& cx, const Cur& 
       }
     }
   }
-  if (up || cx.ext || cur.tok0 + kDecPassTok < cur.cnt) return;
+  if (up || a.ext || a.n > kDecLateCombine || cur.tok0 + kDecPassTok < cur.cnt) return;
   // down tile complete: count it against its 16 columns
   __threadfence();
   __syncwarp();
@@ -552,6 +566,28 @@ __device__ __forceinline__ void decode_epilogue(const DecodeCtx& cx, const Cur& 
   }
 }
 
+// dst[t][c] = bf16(dst[t][c] + sum_j w[t][j] * Yp[inv[t][j]][c]) for one
+// element, j in order; the k row loads are issued before the FMA chain.
+__device__ __forceinline__ void combine_one(const DecodeArgs& a, const int32_t* s_inv, int32_t tk, int32_t c) {
+  uint16_t* d = a.dst + (size_t)tk * a.H + c;
+  float acc = __uint_as_float((uint32_t)*d << 16);
+  for (int32_t j0 = 0; j0 < a.k; j0 += 8) {
+    int32_t r[8];
+    float y[8], w[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int32_t j = j0 + q;
+      r[q] = j < a.k ? s_inv[tk * a.k + j] : -1;
+      y[q] = r[q] >= 0 ? ld_cg_f32(a.Yp + (size_t)r[q] * a.H + c) : 0.f;
+      w[q] = r[q] >= 0 ? a.tw[tk * a.k + j] : 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (r[q] >= 0) acc = __fmaf_rn(w[q], y[q], acc);
+  }
+  *d = f2bf_rn(acc);
+}
+
 __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) decode_kernel(const __grid_constant__ DecodeArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const DecLayout& L = a.L;
@@ -566,19 +602,21 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) decode_kernel(const __gr
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
   float4* partial = reinterpret_cast<float4*>(smem + L.partial);
   int32_t* pcount = reinterpret_cast<int32_t*>(smem + L.pcount);
+  Cur* descs = reinterpret_cast<Cur*>(smem + L.desc);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nthreads = blockDim.x, W = nthreads >> 5;
   const int32_t R = a.n * a.k, E = a.E;
 
-  for (int i = tid; i < 256; i += nthreads) lut[i] = scale_bf16_2p118((uint32_t)i) * 0x10001u;
-  for (int i = tid; i < kDecMaxWarps; i += nthreads) pcount[i] = 0;
   if (!a.ext) {
     for (int32_t i = tid; i < R; i += nthreads) s_ids[i] = a.ids[i];
     for (int32_t i = tid; i < E; i += nthreads) s_counts[i] = 0;
   }
+  for (int i = tid; i < 256; i += nthreads) lut[i] = scale_bf16_2p118((uint32_t)i) * 0x10001u;
+  for (int i = tid; i < kDecMaxWarps; i += nthreads) pcount[i] = 0;
   if (lane == 0) {
-    for (int q = 0; q < kDecMaxSlots; ++q) mbar_init(&bars[warp * kDecMaxSlots + q], 1);
+    // one arrival from the weight copy's expect_tx, 32 from the lanes' activation copies
+    for (int q = 0; q < kDecMaxSlots; ++q) mbar_init(&bars[warp * kDecMaxSlots + q], 33);
     fence_mbar_init();
   }
   __syncthreads();
@@ -598,10 +636,16 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) decode_kernel(const __gr
   __syncthreads();
 
   const int32_t n_act = misc[1], cmax = misc[2];
+  // slot size follows the widest token pass; keep at least two slots per warp
+  const uint32_t nt_cap = (uint32_t)max(1, min(kDecPassTok, cmax));
+  const uint32_t slot_bytes = kDecCK * kTileBytes + nt_cap * kDecActRow;
+  const uint32_t ring_bytes = L.total - L.ring;
+  const int32_t Weff = max(1, min(W, (int32_t)(ring_bytes / (2u * slot_bytes))));
+  const int32_t P = min(kDecMaxSlots, (int32_t)(ring_bytes / ((uint32_t)Weff * slot_bytes)));
+
   DecodeCtx cx(a);
   cx.s_tok = s_tok; cx.s_counts = s_counts; cx.s_off = s_off; cx.s_act = s_act;
-  cx.g_perm = a.g_perm; cx.ext = a.ext;
-  cx.warp = warp; cx.W = W;
+  cx.warp = warp; cx.W = Weff;
   cx.KTu = a.H / 64; cx.KTd = a.I / 64; cx.NTu = a.I / 16; cx.NTd = a.H / 16;
   {
     const int64_t G = gridDim.x, b = blockIdx.x;
@@ -612,28 +656,39 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) decode_kernel(const __gr
     cx.n_dn = (int32_t)(D * (b + 1) / G) - cx.d_lo;
     cx.split = cmax <= kDecPassTok;
     const int64_t TTu = (int64_t)cx.n_up * cx.KTu, TTd = (int64_t)cx.n_dn * cx.KTd;
-    cx.Wu = (int32_t)(TTu < W ? TTu : W);
-    cx.Wd = (int32_t)(TTd < W ? TTd : W);
+    cx.Wu = (int32_t)(TTu < Weff ? TTu : Weff);
+    cx.Wd = (int32_t)(TTd < Weff ? TTd : Weff);
     cx.ura = warp < cx.Wu ? (int32_t)(TTu * warp / cx.Wu) : 0;
     cx.urb = warp < cx.Wu ? (int32_t)(TTu * (warp + 1) / cx.Wu) : 0;
     cx.dra = warp < cx.Wd ? (int32_t)(TTd * warp / cx.Wd) : 0;
     cx.drb = warp < cx.Wd ? (int32_t)(TTd * (warp + 1) / cx.Wd) : 0;
   }
-  const int32_t P = min(kDecMaxSlots, (int32_t)((L.total - L.ring) / ((uint32_t)W * kDecSlotBytes)));
-  uint8_t* ring = smem + L.ring + (size_t)warp * P * kDecSlotBytes;
+  uint8_t* ring = smem + L.ring + (size_t)min(warp, Weff - 1) * P * slot_bytes;
   uint64_t* wbar = bars + warp * kDecMaxSlots;
+  Cur* wdesc = descs + warp * kDecMaxSlots;
   const uint64_t pol = policy_evict_first();
 
-  // prologue: the first P chunks of this warp's sequence in flight, the next
-  // kDecL2Ahead chunks requested into L2
+  // Chunk q of this warp's sequence lives in slot q % P.  Its weights are
+  // requested P chunks ahead; its activations too, except down chunks issued
+  // before the grid barrier, whose activations follow right after it.
   Cur ci;
   cx.enter_phase(ci, 0);
-  Cur cc = ci;
-  int32_t issued = 0;
-  for (; issued < P && ci.ph < 2; ++issued) {
-    if (lane == 0) cx.issue_weights(ci, ring + issued * kDecSlotBytes, &wbar[issued], pol);
+  int32_t issued = 0, acts_issued = 0;
+  bool crossed = false, dead = false;
+  auto issue = [&](int32_t s) {
+    uint8_t* sp = ring + (size_t)s * slot_bytes;
+    if (lane == 0) {
+      wdesc[s] = ci;
+      cx.issue_weights(ci, sp, &wbar[s], pol);
+    }
+    if (ci.ph == 0 || crossed) {
+      cx.issue_acts(ci, lane, sp, &wbar[s]);
+      ++acts_issued;
+    }
     cx.advance(ci);
-  }
+    ++issued;
+  };
+  for (int32_t s = 0; s < P && ci.ph < 2; ++s) issue(s);
   {
     Cur cp = ci;
     for (int q = 0; q < kDecL2Ahead && cp.ph < 2; ++q) {
@@ -641,39 +696,38 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) decode_kernel(const __gr
       cx.advance(cp);
     }
   }
-  uint4 bA[kDecCK][2], bB[kDecCK][2];
-  bool crossed = false, dead = false;
-  if (cc.ph == 0) cx.load_acts(cc, lane, bA);
+  __syncwarp();
+
   int32_t consumed = 0, slot = 0;
   uint32_t phase = 0;
   float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
-
-  // One chunk: bc holds its activation fragments, bn receives the next chunk's.
-  auto step = [&](uint4 (&bc)[kDecCK][2], uint4 (&bn)[kDecCK][2]) -> bool {
-    if (cc.ph == 1 && !crossed) {
+  while (consumed < issued) {
+    const Cur cur = wdesc[slot];
+    if (cur.ph == 1 && !crossed) {
       // every up tile of every CTA is stored before any down tile reads Ap
-      decode_grid_barrier(a, tid, nthreads);
+      decode_grid_barrier(a, tid, nthreads, (int32_t)gridDim.x);
       crossed = true;
-      cx.load_acts(cc, lane, bc);
+      for (int32_t q = acts_issued; q < issued; ++q) {
+        const int32_t s = q % P;
+        cx.issue_acts(wdesc[s], lane, ring + (size_t)s * slot_bytes, &wbar[s]);
+      }
+      acts_issued = issued;
     }
     const bool ok = mbar_wait_sleep(&wbar[slot], phase, a.err);
     if (__any_sync(0xffffffffu, !ok)) {
       dead = true;
-      return false;
+      break;
     }
-    const Cur cur = cc;
-    cx.advance(cc);
-    if (cc.ph == 0 || (cc.ph == 1 && crossed)) cx.load_acts(cc, lane, bn);
-    chunk_mma(ring + slot * kDecSlotBytes, bc, cx.kts(cur), lane, lut, acc, acc2);
+    const uint8_t* sp = ring + (size_t)slot * slot_bytes;
+    const int32_t nt = min(kDecPassTok, cur.cnt - cur.tok0);
+    const uint8_t* act = sp + kDecCK * kTileBytes + min(lane >> 2, nt - 1) * kDecActRow + (lane & 3) * 32;
+    chunk_mma(sp, act, cx.kts(cur), lane, lut, acc, acc2);
     ++consumed;
     __syncwarp();
     if (ci.ph < 2) {
-      if (lane == 0) {
-        fence_proxy_async_smem();
-        cx.issue_weights(ci, ring + slot * kDecSlotBytes, &wbar[slot], pol);
-      }
-      cx.advance(ci);
-      ++issued;
+      if (lane == 0) fence_proxy_async_smem();
+      issue(slot);
+      __syncwarp();
     }
     if (++slot == P) {
       slot = 0;
@@ -689,16 +743,19 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) decode_kernel(const __gr
       }
       decode_epilogue(cx, cur, v, lane, partial, pcount, s_inv, n_act);
     }
-    return true;
-  };
-  while (cc.ph < 2) {
-    if (!step(bA, bB) || cc.ph >= 2) break;
-    if (!step(bB, bA)) break;
   }
-  if (!crossed) decode_grid_barrier(a, tid, nthreads);
+  if (!crossed) decode_grid_barrier(a, tid, nthreads, (int32_t)gridDim.x);
   if (dead) {
     // let this warp's copies still in flight land before the CTA exits
-    for (int32_t c = consumed; c < issued; ++c) mbar_wait_sleep(&wbar[c % P], (uint32_t)((c / P) & 1), a.err);
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    for (int32_t q = consumed; q < issued; ++q) mbar_wait_sleep(&wbar[q % P], (uint32_t)((q / P) & 1), a.err);
+  }
+  if (!a.ext && a.n > kDecLateCombine) {
+    // every down row of every CTA is stored: combine, one element per thread
+    decode_grid_barrier(a, tid, nthreads, 2 * (int32_t)gridDim.x);
+    const int64_t total = (int64_t)a.n * a.H, stride = (int64_t)gridDim.x * nthreads;
+    for (int64_t idx = (int64_t)blockIdx.x * nthreads + tid; idx < total; idx += stride)
+      combine_one(a, s_inv, (int32_t)(idx / a.H), (int32_t)(idx % a.H));
   }
   all_warps_sync(nthreads);
   if (tid == 0) {

@@ -67,11 +67,12 @@ constexpr int kDecCK = 4;              // k-tiles (of 64) per chunk
 constexpr int kDecSlotBytes = kDecCK * kTileBytes;
 constexpr int kDecPassTok = 8;         // tokens per pass over a tile (one n8 MMA block)
 constexpr int kDecL2Ahead = 8;         // chunks past the ring requested into L2 at start
+constexpr int kDecLateCombine = 8;     // larger batches combine after a second grid barrier
 constexpr int kDecMaxPairs = 1024;
 
 // Shared-memory plan of the decode kernel (byte offsets; the host computes it).
 struct DecLayout {
-  uint32_t scale_lut, ids, perm, inv, counts, offsets, act, misc, bars, partial, pcount, ring, total;
+  uint32_t scale_lut, ids, perm, inv, counts, offsets, act, misc, bars, partial, pcount, desc, ring, total;
   uint32_t warps;
 };
 
@@ -95,6 +96,7 @@ inline DecLayout dec_layout(int32_t E, int32_t R, uint32_t budget) {
   L.bars = take(8 * kDecMaxSlots * kDecMaxWarps, 16);
   L.partial = take(2 * kDecMaxWarps * 32 * 16, 128);  // (warp, first/last segment) x lanes x float4
   L.pcount = take(kDecMaxWarps * 4, 16);
+  L.desc = take(kDecMaxWarps * kDecMaxSlots * 48, 16);  // per-slot chunk descriptors
   const uint32_t ring_at = (o + 127) / 128 * 128;
   uint32_t warps = budget > ring_at ? (budget - ring_at) / (2 * kDecSlotBytes) : 0;
   if (warps > (uint32_t)kDecMaxWarps) warps = kDecMaxWarps;
