@@ -2,32 +2,34 @@
 //
 // At one token the layer reads 6 experts x 5.6 MB of NVFP4 weights and almost
 // nothing else, so its time is set by how early and how fast those bytes
-// stream in.  The Zig/CUDA issue "nvfp4 experts cuda: decode kernels stall on
-// load latency; a cp.async ring makes GLM-5.3 decode up to 24% faster, same
-// bits" (#2265) finds such kernels load-latency bound and fixes them with a
-// per-warp shared-memory ring of weight stages filled ahead of use; gllm pull
-// request #91 ("Results") runs experts with at most 32 tokens on a GEMV.  Here
-// one cooperative kernel (one CTA per SM) does the whole layer:
+// stream in.  TensorFold issue #2265 ("Proposal") finds such decode kernels
+// stalled on load latency and keeps, per warp, a ring of shared-memory stages
+// filled asynchronously with the weight words, block scales and input rows;
+// gllm pull request #91 ("Results") runs experts holding at most 32 tokens on
+// a GEMV.  Here one cooperative kernel (one CTA per SM) does the whole layer:
 //
 //   1. warp 0 routes the <= 1024 pairs in shared memory (counts, offsets,
 //      stable permutation), identically in every CTA;
-//   2. the CTA's share of (expert, 16-row tile) items -- up tiles first, then
-//      down tiles -- is cut into sub-items (a tile's k range split over up to
-//      4 warps when the CTA has few tiles) dealt round-robin to its warps.
-//      Every warp streams its own sub-items: its lane 0 issues 1-D bulk copies
-//      of 4-k-tile weight chunks into the warp's private ring, several chunks
-//      ahead, while the lanes load the matching activation fragments from
-//      global memory one chunk ahead; no warp waits on another in the loop;
-//   3. the warp unpacks its codes exactly to bf16 in registers (bit placement
+//   2. the CTA's share of (expert, 16-row tile) items -- up tiles, then down
+//      tiles -- is laid out as one run of 64-wide k-tiles per phase and cut
+//      evenly over the warps (a warp's range may start or end inside a tile);
+//   3. each warp streams its range through a private ring of slots; a slot
+//      holds a chunk of up to 4 weight k-tiles and the matching activation row
+//      segments of up to 8 tokens, all copied by 1-D bulk copies completing on
+//      the slot's mbarrier, several chunks ahead of use; no warp waits on
+//      another in the loop;
+//   4. the warp unpacks its codes exactly to bf16 in registers (bit placement
 //      + one bf16 multiply by the e4m3 scale, see below) and feeds them as A
 //      fragments of warp-level bf16 MMAs with fp32 accumulation; the last warp
-//      to finish a split tile sums the partial tiles in k order and writes it:
+//      holding part of a tile sums the parts in warp order and writes it:
 //      relu^2 + bf16 rounding fused into the up store, fp32 rows for down;
-//   4. one grid barrier (a single arrival per CTA) separates up from down; the
-//      weight chunks of the first down tiles are already in flight across it;
-//   5. a per-16-column counter finds the last warp to finish a column block;
-//      that warp applies the WeightedRowSum to those columns of dst for every
-//      token (fixed j order, one fma each, no atomics on data).
+//   5. one grid barrier (a single arrival per CTA) separates up from down; the
+//      weight chunks of the first down tiles are already in flight across it,
+//      their activation rows (the relu^2 rows) are requested right after it;
+//   6. the WeightedRowSum onto dst (fixed j order, one fma each, no atomics on
+//      data): for up to 8 tokens the last warp to finish a 16-column block of
+//      down tiles applies it to those columns, for more tokens every thread
+//      takes one element after a second grid barrier.
 //
 // The same kernel also serves the experts with few rows inside a large batch
 // (external-routing mode): it then takes the counts, offsets and permutation
@@ -160,6 +162,9 @@ __device__ __forceinline__ int32_t ld_acquire_gpu(const int32_t* p) {
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
+__device__ __forceinline__ void red_release_gpu_add(int32_t* p, int32_t v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 __device__ __forceinline__ void all_warps_sync(int nthreads) {
   asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
 }
@@ -184,14 +189,6 @@ struct __align__(16) Cur {
 
 __device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-// The barrier receives one arrival once all of this thread's earlier cp.async
-// copies have landed (counted in the barrier's expected arrivals).
-__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 // Ring slot layout: kDecCK weight tiles, then the chunk's activation rows:
@@ -284,36 +281,29 @@ struct DecodeCtx {
     return base + ((size_t)((size_t)c.e * NT + c.rt) * KT + c.kt) * kTileBytes;
   }
   __device__ __forceinline__ int32_t kts(const Cur& c) const { return min(kDecCK, c.kt_end - c.kt); }
-  // Lane 0 only: bulk-copy the chunk's weight tiles into its ring slot.
+  // Lane 0 only: declare the chunk's bytes (weight tiles and activation rows,
+  // the latter possibly issued later) and bulk-copy the weight tiles.
   __device__ __forceinline__ void issue_weights(const Cur& c, uint8_t* slot, uint64_t* bar, uint64_t pol) const {
-    const uint32_t bytes = (uint32_t)kts(c) * kTileBytes;
-    mbar_arrive_expect_tx(bar, bytes);
-    bulk_g2s_hint(slot, chunk_src(c), bytes, bar, pol);
+    const uint32_t n_kt = (uint32_t)kts(c);
+    const uint32_t nt = (uint32_t)min(kDecPassTok, c.cnt - c.tok0);
+    mbar_arrive_expect_tx(bar, n_kt * (kTileBytes + nt * 128u));
+    bulk_g2s_hint(slot, chunk_src(c), n_kt * kTileBytes, bar, pol);
   }
-  // All lanes: copy the chunk's activation rows (16 B per lane and copy) into
-  // the slot, then arrive on its barrier when they have landed.
+  // Lanes g < nt: bulk-copy token column g's activation row segment (kts x 64
+  // bf16) into the slot; it completes on the slot's barrier.
   __device__ __forceinline__ void issue_acts(const Cur& c, int lane, uint8_t* slot, uint64_t* bar) const {
-    const int g = lane >> 2, t = lane & 3;
     const int32_t nt = min(kDecPassTok, c.cnt - c.tok0);
-    if (g < nt) {
-      const int32_t pr = c.off + c.tok0 + g;
+    if (lane < nt) {
+      const int32_t pr = c.off + c.tok0 + lane;
       const uint16_t* src;
       if (c.ph == 0) {
         const int32_t tok = a.ext ? __ldg(a.g_perm + pr) / a.k : s_tok[pr];
-        src = a.x + (size_t)tok * a.H + c.kt * 64 + 16 * t;
+        src = a.x + (size_t)tok * a.H + c.kt * 64;
       } else {
-        src = a.Ap + (size_t)pr * a.I + c.kt * 64 + 16 * t;
+        src = a.Ap + (size_t)pr * a.I + c.kt * 64;
       }
-      uint8_t* dst = slot + kDecCK * kTileBytes + g * kDecActRow + t * 32;
-      const int32_t n_kt = kts(c);
-#pragma unroll
-      for (int kt = 0; kt < kDecCK; ++kt)
-        if (kt < n_kt) {
-          cp_async16(dst + kt * 128, src + kt * 64);
-          cp_async16(dst + kt * 128 + 16, src + kt * 64 + 8);
-        }
+      bulk_g2s(slot + kDecCK * kTileBytes + lane * kDecActRow, src, (uint32_t)kts(c) * 128u, bar);
     }
-    cp_async_arrive(bar);
   }
 };
 
@@ -463,19 +453,18 @@ __device__ __forceinline__ void decode_select(const DecodeArgs& a, int lane, int
 __device__ __forceinline__ void decode_grid_barrier(const DecodeArgs& a, int tid, int nthreads, int32_t want) {
   all_warps_sync(nthreads);
   if (tid == 0) {
-    __threadfence();
-    atomicAdd(&a.grid_bar[0], 1);
+    // release: this CTA's stores (ordered before by the CTA barrier) become
+    // visible with the arrival; acquire: other CTAs' stores are visible after
+    red_release_gpu_add(&a.grid_bar[0], 1);
     if (ld_acquire_gpu(&a.grid_bar[0]) < want) {
       const uint64_t t0 = globaltimer_ns();
       while (ld_acquire_gpu(&a.grid_bar[0]) < want) {
-        __nanosleep(32);
         if (globaltimer_ns() - t0 > kWaitLimitNs) {
           atomicOr(a.err, kFlagTimeout);
           break;
         }
       }
     }
-    __threadfence();
   }
   all_warps_sync(nthreads);
 }
@@ -615,8 +604,8 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) decode_kernel(const __gr
   for (int i = tid; i < 256; i += nthreads) lut[i] = scale_bf16_2p118((uint32_t)i) * 0x10001u;
   for (int i = tid; i < kDecMaxWarps; i += nthreads) pcount[i] = 0;
   if (lane == 0) {
-    // one arrival from the weight copy's expect_tx, 32 from the lanes' activation copies
-    for (int q = 0; q < kDecMaxSlots; ++q) mbar_init(&bars[warp * kDecMaxSlots + q], 33);
+    // one arrival: lane 0's expect_tx covering the weight and activation copies
+    for (int q = 0; q < kDecMaxSlots; ++q) mbar_init(&bars[warp * kDecMaxSlots + q], 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -689,13 +678,6 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) decode_kernel(const __gr
     ++issued;
   };
   for (int32_t s = 0; s < P && ci.ph < 2; ++s) issue(s);
-  {
-    Cur cp = ci;
-    for (int q = 0; q < kDecL2Ahead && cp.ph < 2; ++q) {
-      if (lane == 0) prefetch_l2_bulk(cx.chunk_src(cp), (uint32_t)cx.kts(cp) * kTileBytes);
-      cx.advance(cp);
-    }
-  }
   __syncwarp();
 
   int32_t consumed = 0, slot = 0;
@@ -717,6 +699,14 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) decode_kernel(const __gr
     if (__any_sync(0xffffffffu, !ok)) {
       dead = true;
       break;
+    }
+    if (consumed == 0 && lane == 0) {
+      // once the first chunk has landed, ask L2 for the chunks past the ring
+      Cur cp = ci;
+      for (int q = 0; q < kDecL2Ahead && cp.ph < 2; ++q) {
+        prefetch_l2_bulk(cx.chunk_src(cp), (uint32_t)cx.kts(cp) * kTileBytes);
+        cx.advance(cp);
+      }
     }
     const uint8_t* sp = ring + (size_t)slot * slot_bytes;
     const int32_t nt = min(kDecPassTok, cur.cnt - cur.tok0);
@@ -747,7 +737,6 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) decode_kernel(const __gr
   if (!crossed) decode_grid_barrier(a, tid, nthreads, (int32_t)gridDim.x);
   if (dead) {
     // let this warp's copies still in flight land before the CTA exits
-    asm volatile("cp.async.wait_all;" ::: "memory");
     for (int32_t q = consumed; q < issued; ++q) mbar_wait_sleep(&wbar[q % P], (uint32_t)((q / P) & 1), a.err);
   }
   if (!a.ext && a.n > kDecLateCombine) {

@@ -1,10 +1,9 @@
 // gemv.cu -- NVFP4 weight-streaming path for experts with few packed rows.
 //
 // gllm pull request #91, "Results": experts holding at most 32 tokens run an
-// NVFP4 GEMV instead of the tensor-core GEMM; the Zig/CUDA issue #2265 ("nvfp4
-// experts cuda: decode kernels stall on load latency ...") measures the same
-// kind of kernel as load-latency bound and keeps the k order of each row's sum
-// fixed so every output bit stays the same.
+// NVFP4 GEMV instead of the tensor-core GEMM; TensorFold issue #2265
+// ("Proposal") measures the same kind of kernel as load-latency bound and keeps
+// the k order of each row's sum fixed so every output bit stays the same.
 //
 // One launch covers every expert that takes this path.  A warp owns one
 // weight row (expert e, output feature n) at a time and streams it straight
