@@ -55,6 +55,8 @@ struct moe_nvfp4 {
   float *up_g = nullptr, *dn_g = nullptr;
   // the same weights in fragment-tile order for the single-launch small-batch path
   uint8_t *up_tiles = nullptr, *dn_tiles = nullptr;
+  // and in packed 128-row blocks for the grouped GEMM
+  uint8_t *up_blocks = nullptr, *dn_blocks = nullptr;
   int32_t *col_done = nullptr, *grid_bar = nullptr;
   // workspace (max_tokens)
   int32_t *counts = nullptr, *offsets = nullptr, *perm_pair = nullptr, *inv = nullptr, *err = nullptr;
@@ -65,7 +67,7 @@ struct moe_nvfp4 {
   int32_t* ids_stage = nullptr;
   float* w_stage = nullptr;
   // tensor maps
-  CUtensorMap tm_xp{}, tm_ap{}, tm_up_codes{}, tm_dn_codes{};
+  CUtensorMap tm_xp{}, tm_ap{};  // 192-row activation tiles of the grouped GEMM
   int32_t last_n = 0;
   // per-kernel timing
   bool timing = false;
@@ -82,7 +84,7 @@ void free_handle(moe_nvfp4* h) {
   void* ptrs[] = {h->up_codes, h->up_scales, h->dn_codes, h->dn_scales, h->up_g,      h->dn_g,
                   h->counts,   h->offsets,   h->perm_pair, h->inv,      h->err,       h->Xp,
                   h->Ap,       h->Yp,        h->x_stage,   h->dst_stage, h->ids_stage, h->w_stage,
-                  h->up_tiles, h->dn_tiles,  h->col_done,  h->grid_bar};
+                  h->up_tiles, h->dn_tiles,  h->col_done,  h->grid_bar,  h->up_blocks, h->dn_blocks};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   for (auto& s : h->slots) {
@@ -207,6 +209,8 @@ moe_status moe_nvfp4_create(const moe_nvfp4_config* config, const moe_nvfp4_weig
   TRY(cudaMalloc(&h->w_stage, Rr * sizeof(float)));
   TRY(cudaMalloc(&h->up_tiles, mat_codes + mat_scales));
   TRY(cudaMalloc(&h->dn_tiles, mat_codes + mat_scales));
+  TRY(cudaMalloc(&h->up_blocks, gemm_blocks_bytes((int32_t)E, (int32_t)I, (int32_t)H)));
+  TRY(cudaMalloc(&h->dn_blocks, gemm_blocks_bytes((int32_t)E, (int32_t)H, (int32_t)I)));
   TRY(cudaMalloc(&h->col_done, (H / 16) * sizeof(int32_t)));
   TRY(cudaMalloc(&h->grid_bar, 2 * sizeof(int32_t)));
   TRY(cudaMemcpyAsync(h->up_codes, w->up_codes, mat_codes, cudaMemcpyDeviceToDevice, s));
@@ -224,10 +228,10 @@ moe_status moe_nvfp4_create(const moe_nvfp4_config* config, const moe_nvfp4_weig
   TRY(cudaMemsetAsync(h->grid_bar, 0, 2 * sizeof(int32_t), s));
   TRY(launch_repack_frag(h->up_codes, h->up_scales, (int32_t)E, (int32_t)I, (int32_t)H, h->up_tiles, s));
   TRY(launch_repack_frag(h->dn_codes, h->dn_scales, (int32_t)E, (int32_t)H, (int32_t)I, h->dn_tiles, s));
-  TRY(make_tmap_act(&h->tm_xp, h->Xp, Rr, H));
-  TRY(make_tmap_act(&h->tm_ap, h->Ap, Rr, I));
-  TRY(make_tmap_codes(&h->tm_up_codes, h->up_codes, E * I, H));
-  TRY(make_tmap_codes(&h->tm_dn_codes, h->dn_codes, E * H, I));
+  TRY(launch_repack_gemm(h->up_codes, h->up_scales, (int32_t)E, (int32_t)I, (int32_t)H, h->up_blocks, s));
+  TRY(launch_repack_gemm(h->dn_codes, h->dn_scales, (int32_t)E, (int32_t)H, (int32_t)I, h->dn_blocks, s));
+  TRY(make_tmap_act_rows(&h->tm_xp, h->Xp, Rr, H, 192));
+  TRY(make_tmap_act_rows(&h->tm_ap, h->Ap, Rr, I, 192));
   TRY(cudaStreamSynchronize(s));
 #undef TRY
   *out = h;
@@ -331,7 +335,7 @@ static moe_status forward_impl(moe_nvfp4* h, const uint16_t* x, const int32_t* i
     e = launch_gemv(g, s, pdl);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
-  GemmArgs m{};
+  Gemm2Args m{};
   m.counts = h->counts;
   m.offsets = h->offsets;
   m.G = E;
@@ -339,13 +343,13 @@ static moe_status forward_impl(moe_nvfp4* h, const uint16_t* x, const int32_t* i
   m.err = h->err;
   if (gemm) {
     TimedLaunch tl(h, s, kKGemmUp);
-    m.scales = h->up_scales;
+    m.blocks = h->up_blocks;
     m.global = h->up_g;
     m.N = I;
     m.K = H;
     m.out = h->Ap;
     m.epilogue = 1;
-    e = launch_gemm(h->tm_xp, h->tm_up_codes, m, h->num_sms, s, pdl);
+    e = launch_gemm2(h->tm_xp, m, h->num_sms, s, pdl);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
   if (!small_done) {
@@ -364,13 +368,13 @@ static moe_status forward_impl(moe_nvfp4* h, const uint16_t* x, const int32_t* i
   }
   if (gemm) {
     TimedLaunch tl(h, s, kKGemmDown);
-    m.scales = h->dn_scales;
+    m.blocks = h->dn_blocks;
     m.global = h->dn_g;
     m.N = H;
     m.K = I;
     m.out = h->Yp;
     m.epilogue = 0;
-    e = launch_gemm(h->tm_ap, h->tm_dn_codes, m, h->num_sms, s, pdl);
+    e = launch_gemm2(h->tm_ap, m, h->num_sms, s, pdl);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
   {

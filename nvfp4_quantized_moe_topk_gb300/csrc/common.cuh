@@ -247,4 +247,41 @@ __host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N) {
          | ((M >> 4) << 24);  // M / 16
 }
 
+// ------------------------------------------------- bit-placed NVFP4 codes
+// The fragment-tile and GEMM-block weight layouts store each 32-bit word of 8
+// e2m1 codes bit-placed so that every bf16 pair is one or two shifts and a
+// mask away: a code lands as sign | exponent (2 bits) | mantissa (1 bit) in the
+// bf16 sign, low exponent and top mantissa bits, i.e. as e2m1 * 2^-126, and
+// one bf16 multiply by (e4m3 scale * 2^118) gives the exact weight * 2^-8.
+// Bit position of code bit `b` (0 mantissa, 1 exponent lsb, 2 exponent msb,
+// 3 sign) of the low (h = 0) or high (h = 1) element of pair slot p (0..3) of
+// a 32-bit word.  Slots 0..2 are the translates of {6,7,8,15 | 22,23,24,31} by
+// 0, -3, -6; slot 3 takes the remaining bits {10,11,13,14 | 26,27,29,30}.
+__host__ __device__ constexpr int code_bit_pos(int p, int h, int b) {
+  return p < 3 ? (b < 3 ? 6 + b : 15) - 3 * p + 16 * h
+               : (b == 0 ? 10 : b == 1 ? 11 : b == 2 ? 13 : 14) + 16 * h;
+}
+
+// bf16 of (e4m3 byte value) * 2^118, exact (|value| <= 448 keeps it finite).
+__device__ __forceinline__ uint32_t scale_bf16_2p118(uint32_t b) {
+  const uint32_t s = (b >> 7) & 1u, e = (b >> 3) & 15u, m = b & 7u;
+  const float v = (e == 0) ? (float)m * 0x1p109f : __uint_as_float(((e + 238u) << 23) | (m << 20));
+  return (uint32_t)f2bf_rn(v) | (s << 15);
+}
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// The four bf16 pairs held by one 32-bit word of bit-placed codes, each value
+// e2m1 * 2^-126.
+__device__ __forceinline__ void unpack_word(uint32_t w, uint32_t& p0, uint32_t& p1, uint32_t& p2, uint32_t& p3) {
+  constexpr uint32_t M = 0x81C081C0u;
+  p0 = w & M;
+  p1 = (w << 3) & M;
+  p2 = (w << 6) & M;
+  p3 = ((w >> 4) & 0x00C000C0u) | ((w >> 5) & 0x01000100u) | ((w << 1) & 0x80008000u);
+}
+
+
 }  // namespace moe

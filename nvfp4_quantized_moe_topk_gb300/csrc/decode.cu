@@ -56,15 +56,6 @@
 namespace moe {
 
 // ------------------------------------------------------------------ repack
-// Bit position of code bit `b` (0 mantissa, 1 exponent lsb, 2 exponent msb,
-// 3 sign) of the low (h = 0) or high (h = 1) element of pair slot p (0..3) of
-// a 32-bit word.  Slots 0..2 are the translates of {6,7,8,15 | 22,23,24,31} by
-// 0, -3, -6; slot 3 takes the remaining bits {10,11,13,14 | 26,27,29,30}.
-__host__ __device__ constexpr int code_bit_pos(int p, int h, int b) {
-  return p < 3 ? (b < 3 ? 6 + b : 15) - 3 * p + 16 * h
-               : (b == 0 ? 10 : b == 1 ? 11 : b == 2 ? 13 : 14) + 16 * h;
-}
-
 __global__ void repack_frag_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
                                    int32_t G, int32_t N, int32_t K, uint8_t* __restrict__ out) {
   const int32_t KT = K / 64, NT = N / 16;
@@ -123,17 +114,6 @@ cudaError_t launch_repack_frag(const uint8_t* codes, const uint8_t* scales, int3
 }
 
 // ------------------------------------------------------------------ helpers
-// bf16 of (e4m3 byte value) * 2^118, exact (|value| <= 448 keeps it finite).
-__device__ __forceinline__ uint32_t scale_bf16_2p118(uint32_t b) {
-  const uint32_t s = (b >> 7) & 1u, e = (b >> 3) & 15u, m = b & 7u;
-  const float v = (e == 0) ? (float)m * 0x1p109f : __uint_as_float(((e + 238u) << 23) | (m << 20));
-  return (uint32_t)f2bf_rn(v) | (s << 15);
-}
-__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                                uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -167,16 +147,6 @@ __device__ __forceinline__ void red_release_gpu_add(int32_t* p, int32_t v) {
 }
 __device__ __forceinline__ void all_warps_sync(int nthreads) {
   asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
-}
-
-// The four bf16 pairs held by one 32-bit word of bit-placed codes, each value
-// e2m1 * 2^-126.
-__device__ __forceinline__ void unpack_word(uint32_t w, uint32_t& p0, uint32_t& p1, uint32_t& p2, uint32_t& p3) {
-  constexpr uint32_t M = 0x81C081C0u;
-  p0 = w & M;
-  p1 = (w << 3) & M;
-  p2 = (w << 6) & M;
-  p3 = ((w >> 4) & 0x00C000C0u) | ((w >> 5) & 0x01000100u) | ((w << 1) & 0x80008000u);
 }
 
 // ------------------------------------------------------------ work cursor

@@ -477,11 +477,15 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 }
 
 cudaError_t make_tmap_act(CUtensorMap* map, const void* base, uint64_t rows, uint64_t K) {
+  return make_tmap_act_rows(map, base, rows, K, kBM);
+}
+
+cudaError_t make_tmap_act_rows(CUtensorMap* map, const void* base, uint64_t rows, uint64_t K, uint32_t box_rows) {
   auto enc = get_encode();
   if (!enc) return cudaErrorNotSupported;
   const cuuint64_t dims[2] = {K, rows};
   const cuuint64_t strides[1] = {K * 2};
-  const cuuint32_t box[2] = {kBK, kBM};
+  const cuuint32_t box[2] = {kBK, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

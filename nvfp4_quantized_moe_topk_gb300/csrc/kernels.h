@@ -58,6 +58,27 @@ struct GemmArgs {
 cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int num_sms,
                         cudaStream_t s, bool pdl);
 
+// ------------------------------------------- grouped GEMM, A operand in TMEM
+// Packed weight blocks [G][ceil(N/128)][K/64] of 4608 bytes (gemm2.cu).
+constexpr uint32_t kGemmBlockBytes = 128 * 32 + 128 * 4;
+cudaError_t launch_repack_gemm(const uint8_t* codes, const uint8_t* scales, int32_t G, int32_t N, int32_t K,
+                               uint8_t* out, cudaStream_t s);
+size_t gemm_blocks_bytes(int32_t G, int32_t N, int32_t K);
+struct Gemm2Args {
+  const uint8_t* blocks;   // packed weight blocks of the G groups
+  const float* global;     // [G] per-group alpha
+  const int32_t* counts;   // [G] rows per group
+  const int32_t* offsets;  // [G+1]
+  int32_t G, N, K;
+  int32_t min_rows;        // groups with count > min_rows take this path
+  void* out;               // [rows][N]: fp32 (epilogue 0) or bf16 relu^2 (epilogue 1)
+  int32_t epilogue;
+  int32_t* err;
+};
+// tmX: bf16 activations [rows][K], box 64 x 192, 128-byte swizzle.
+cudaError_t launch_gemm2(const CUtensorMap& tmX, const Gemm2Args& a, int num_sms, cudaStream_t s, bool pdl);
+cudaError_t make_tmap_act_rows(CUtensorMap* map, const void* base, uint64_t rows, uint64_t K, uint32_t box_rows);
+
 // ------------------------------------------------------- decode (small batch)
 // Fragment-tile weight layout and the single-launch small-batch layer (decode.cu).
 constexpr int kTileBytes = 576;        // 16 rows x 64 k: 512 code bytes + 64 scale bytes

@@ -122,3 +122,28 @@ def test_prefill_4314_sampled(dev):
 def test_prefill_16384_sampled(dev):
     wl = W.generate("prefill-16384")
     _layer_vs_oracle(wl, dev, 0, sample=[(0, 4), (9000, 9004), (16380, 16384)])
+
+
+@pytest.mark.parametrize("n,H,I,E,k,T,seed", [(500, 256, 320, 3, 2, 1, 23), (250, 384, 192, 2, 1, 16, 24)])
+def test_grouped_gemm_token_tiles_and_ragged_features(dev, n, H, I, E, k, T, seed):
+    """Experts of a few hundred rows span several 192-row token tiles (the last
+    one ragged), and I = 320 / H = 384 leave a partial 128-feature block; the
+    relu^2 rows and fp32 down rows must match the oracle as well as dst."""
+    import torch
+
+    wl = W.small_custom(n, H, I, E, k, seed)
+    layer = make_layer(wl, dev, gemv_max_rows=T)
+    got = run_forward(layer, wl, dev)
+    assert layer.device_error() == 0
+    ref = oracle.moe_forward(wl, intermediates=True)
+    ok, err, rms = layer_tolerance_check(got, ref.dst)
+    assert ok, (err, rms)
+    a = torch.empty((wl.R, wl.I), dtype=torch.int16, device=dev)
+    y = torch.empty((wl.R, wl.H), dtype=torch.float32, device=dev)
+    layer.debug_intermediates(a, y)
+    torch.cuda.synchronize()
+    ok_a, ea, ra = layer_tolerance_check(a.cpu().numpy().view(np.uint16), ref.a_rows)
+    assert ok_a, ("relu^2 rows", ea, ra)
+    ok_y, ey, ry = fp_tolerance_check(y.cpu().numpy(), ref.y_rows)
+    assert ok_y, ("down rows", ey, ry)
+    layer.close()
