@@ -78,7 +78,8 @@ def algorithmic_work(wl, ids_list, T):
     per = {"gemv_up": [0.0, 0.0], "gemv_down": [0.0, 0.0], "gemm_up": [0.0, 0.0], "gemm_down": [0.0, 0.0],
            "combine": [0.0, 0.0], "routing": [0.0, 0.0], "gather": [0.0, 0.0]}
     mat_bytes = H * I // 2 + H * I // 16
-    gemm_path = n > T
+    single = decode_single_launch(n, k, T)
+    gemm_path = not single and n > T
     for ids in ids_list:
         c = np.bincount(ids.ravel(), minlength=E)
         for e in range(E):
@@ -104,7 +105,7 @@ def algorithmic_work(wl, ids_list, T):
         # experts at or below the threshold run in one streaming launch (both projections)
         out["small_experts"] = (out["gemv_up"][0] + out["gemv_down"][0], out["gemv_up"][1] + out["gemv_down"][1])
         del out["gemv_up"], out["gemv_down"]
-    if decode_single_launch(n, k, T):
+    if single:
         # the whole layer is one kernel: its bytes are those of the four steps it fuses
         parts = ("routing", "gemv_up", "gemv_down", "combine")
         out = {"decode": (sum(out[p][0] for p in parts), sum(out[p][1] for p in parts))}
@@ -113,7 +114,7 @@ def algorithmic_work(wl, ids_list, T):
 
 def decode_single_launch(n, k, T):
     """Whether the library runs this batch as its one-launch small-batch kernel."""
-    return n <= T and n * k <= 1024
+    return n <= 64 and n * k <= 1024
 
 
 # ----------------------------------------------------------------- clocks
@@ -259,7 +260,7 @@ def run_ours(args):
     api.load(build_if_missing=True)
     cfg = W.CONFIGS[args.workload]
     wl = W.generate(args.workload)
-    T = args.gemv_max_rows if args.gemv_max_rows > 0 else 32
+    T = args.gemv_max_rows if args.gemv_max_rows > 0 else 8
     routings = [(wl.topk_ids, wl.topk_weights)] + [
         W.make_routing(wl.n, wl.E, wl.k, cfg["bias_sigma"], seed=5000 + 97 * i) for i in range(1, N_ROUTINGS)]
 

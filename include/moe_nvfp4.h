@@ -80,10 +80,15 @@ typedef struct moe_nvfp4_config {
   int32_t n_experts;     /* E */
   int32_t top_k;         /* k */
   int32_t max_tokens;    /* largest n a forward may be called with */
-  int32_t gemv_max_rows; /* experts with at most this many rows take the
-                            weight-streaming (GEMV) path, larger ones the
-                            tensor-core grouped GEMM; <= 0 selects 32, the
-                            threshold pull request #91 names in "Results" */
+  int32_t gemv_max_rows; /* in a batch that is not run as one launch (see
+                            moe_nvfp4_forward), experts with at most this many
+                            rows take the weight-streaming path, larger ones
+                            the tensor-core grouped GEMM; <= 0 selects 8 (pull
+                            request #91, "Results", uses 32 for its GEMV; 8 is
+                            the measured best here for the 4314-token
+                            prefill) */
+  int32_t single_max_tokens; /* batches with n <= this and n * k <= 1024 run
+                                as one launch; 0 selects 64, < 0 never */
 } moe_nvfp4_config;
 
 typedef struct moe_nvfp4_weights { /* device pointers, layouts as above */
@@ -118,9 +123,13 @@ MOE_API moe_status moe_nvfp4_destroy(moe_nvfp4_t handle);
  *   topk_ids     device int32 [n][k]
  *   topk_weights device fp32 [n][k], used as given (no renormalisation)
  *   dst          device bf16 [n][H], read and updated in place
- * Enqueues the routing, the expert GEMV/GEMM kernels and the combine on
- * `stream`; no host synchronisation, no allocation, no host read of device
- * data.  A handle's workspace serves one forward at a time: calls on one
+ * A batch with n <= single_max_tokens (default 64) and n * k <= 1024 runs as
+ * one cooperative launch
+ * (routing, both projections and the combine in one kernel, one CTA per SM);
+ * a larger one enqueues the routing, the gather, the streaming kernel for
+ * experts with at most gemv_max_rows rows, the tensor-core grouped GEMMs and
+ * the combine on `stream`.  No host synchronisation, no allocation, no host
+ * read of device data.  A handle's workspace serves one forward at a time: calls on one
  * stream are ordered; concurrent streams need separate handles.  n = 0
  * returns MOE_OK and enqueues nothing.  Results are bitwise deterministic for
  * a given handle configuration.

@@ -38,7 +38,8 @@ class MoeError(RuntimeError):
 
 class Config(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int32), ("inter", ctypes.c_int32), ("n_experts", ctypes.c_int32),
-                ("top_k", ctypes.c_int32), ("max_tokens", ctypes.c_int32), ("gemv_max_rows", ctypes.c_int32)]
+                ("top_k", ctypes.c_int32), ("max_tokens", ctypes.c_int32), ("gemv_max_rows", ctypes.c_int32),
+                ("single_max_tokens", ctypes.c_int32)]
 
 
 class Weights(ctypes.Structure):
@@ -119,11 +120,11 @@ class MoeLayer:
     """A created layer (``moe_nvfp4_create``); weights are copied into the handle."""
 
     def __init__(self, hidden, inter, n_experts, top_k, max_tokens, up_codes, up_scales, down_codes, down_scales,
-                 up_global, down_global, gemv_max_rows: int = 0, stream=None):
+                 up_global, down_global, gemv_max_rows: int = 0, single_max_tokens: int = 0, stream=None):
         L = load()
         self.hidden, self.inter, self.n_experts, self.top_k = hidden, inter, n_experts, top_k
         self.max_tokens = max_tokens
-        cfg = Config(hidden, inter, n_experts, top_k, max_tokens, gemv_max_rows)
+        cfg = Config(hidden, inter, n_experts, top_k, max_tokens, gemv_max_rows, single_max_tokens)
         w = Weights(_ptr(up_codes), _ptr(up_scales), _ptr(down_codes), _ptr(down_scales), _ptr(up_global),
                     _ptr(down_global))
         h = ctypes.c_void_p()

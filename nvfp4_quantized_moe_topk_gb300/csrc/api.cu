@@ -7,13 +7,18 @@
 // remained of the host cost, so forward allocates nothing and never waits),
 // tensor-map construction, and the launch sequence of one forward:
 //
-//   routing -> [gather] -> up: GEMV (small experts) + [tcgen05 GEMM (large)]
-//           -> down: GEMV + [tcgen05 GEMM] -> WeightedRowSum
+//   n <= single_max_tokens (64) and n*k <= 1024: one cooperative launch of the streaming kernel
+//   (routing, up, relu^2, down and the combine in one kernel)
+//   otherwise: routing -> gather -> streaming kernel for experts with at most
+//   T rows (both projections) -> tcgen05 grouped GEMM up -> grouped GEMM down
+//   -> WeightedRowSum
 //
 // chained with programmatic dependent launch so each kernel's prologue
 // overlaps its predecessor's tail.  The GEMM kernels are enqueued only when
-// some expert can exceed the GEMV threshold (n > threshold); which experts
-// take which path is decided on the device from the routing counts.
+// some expert can exceed the threshold T (n > T); which experts take which
+// path is decided on the device from the routing counts.  When T is set so
+// large that no expert can exceed it and the batch is too large for one
+// launch, the GEMV kernels serve every expert.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -49,7 +54,8 @@ struct moe_nvfp4 {
   moe_nvfp4_config cfg{};
   int device = 0;
   int num_sms = 0;
-  int threshold = 32;
+  int threshold = 8;
+  int single_max_tokens = kDecMaxTokens;
   // library-owned weights
   uint8_t *up_codes = nullptr, *up_scales = nullptr, *dn_codes = nullptr, *dn_scales = nullptr;
   float *up_g = nullptr, *dn_g = nullptr;
@@ -178,7 +184,8 @@ moe_status moe_nvfp4_create(const moe_nvfp4_config* config, const moe_nvfp4_weig
   h->cfg = c;
   h->device = dev;
   h->num_sms = device_sms(dev);
-  h->threshold = c.gemv_max_rows > 0 ? c.gemv_max_rows : 32;
+  h->threshold = c.gemv_max_rows > 0 ? c.gemv_max_rows : 8;
+  h->single_max_tokens = c.single_max_tokens == 0 ? kDecMaxTokens : c.single_max_tokens;
   const size_t H = c.hidden, I = c.inter, E = c.n_experts;
   const size_t R = (size_t)c.max_tokens * c.top_k, Rr = R > 0 ? R : 1;
   const size_t mat_codes = E * H * I / 2, mat_scales = E * H * I / 16;
@@ -281,7 +288,7 @@ static moe_status forward_impl(moe_nvfp4* h, const uint16_t* x, const int32_t* i
   d.I = I;
   d.E = E;
   d.k = k;
-  if (!gemm && R <= kDecMaxPairs) {
+  if (n <= h->single_max_tokens && R <= kDecMaxPairs) {
     // the whole layer in one launch
     d.L = decode_layout(E, R);
     if (d.L.warps >= 4) {

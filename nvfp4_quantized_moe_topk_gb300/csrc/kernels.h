@@ -89,7 +89,8 @@ constexpr int kDecSlotBytes = kDecCK * kTileBytes;
 constexpr int kDecPassTok = 8;         // tokens per pass over a tile (one n8 MMA block)
 constexpr int kDecL2Ahead = 8;         // chunks past the ring requested into L2 at start
 constexpr int kDecLateCombine = 8;     // larger batches combine after a second grid barrier
-constexpr int kDecMaxPairs = 1024;
+constexpr int kDecMaxPairs = 1024;     // batches with at most this many pairs
+constexpr int kDecMaxTokens = 64;      // and tokens run as one launch
 
 // Shared-memory plan of the decode kernel (byte offsets; the host computes it).
 struct DecLayout {

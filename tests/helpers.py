@@ -17,13 +17,15 @@ def bf16_from_dev(t) -> np.ndarray:
     return t.cpu().numpy().view(np.uint16)
 
 
-def make_layer(wl, dev, max_tokens=None, gemv_max_rows=0, stream=None):
+def make_layer(wl, dev, max_tokens=None, gemv_max_rows=0, stream=None, single_max_tokens=0):
+    """single_max_tokens=-1 forces the multi-kernel path (routing, gather,
+    streaming kernel for small experts, grouped GEMMs, combine)."""
     from nvfp4_quantized_moe_topk_gb300 import api
 
     return api.MoeLayer(wl.H, wl.I, wl.E, wl.k, wl.n if max_tokens is None else max_tokens,
                         to_dev(wl.up_codes, dev), to_dev(wl.up_scales, dev), to_dev(wl.down_codes, dev),
                         to_dev(wl.down_scales, dev), to_dev(wl.up_global, dev), to_dev(wl.down_global, dev),
-                        gemv_max_rows=gemv_max_rows, stream=stream)
+                        gemv_max_rows=gemv_max_rows, single_max_tokens=single_max_tokens, stream=stream)
 
 
 def run_forward(layer, wl, dev, stream=None):

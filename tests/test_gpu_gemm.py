@@ -85,7 +85,7 @@ def test_random_within_tolerance(dev, M, N, K, seed):
 
 
 def _layer_vs_oracle(wl, dev, T, sample=None):
-    layer = make_layer(wl, dev, gemv_max_rows=T)
+    layer = make_layer(wl, dev, gemv_max_rows=T, single_max_tokens=-1)
     got = run_forward(layer, wl, dev)
     assert layer.device_error() == 0
     if sample is None:
@@ -132,7 +132,7 @@ def test_grouped_gemm_token_tiles_and_ragged_features(dev, n, H, I, E, k, T, see
     import torch
 
     wl = W.small_custom(n, H, I, E, k, seed)
-    layer = make_layer(wl, dev, gemv_max_rows=T)
+    layer = make_layer(wl, dev, gemv_max_rows=T, single_max_tokens=-1)
     got = run_forward(layer, wl, dev)
     assert layer.device_error() == 0
     ref = oracle.moe_forward(wl, intermediates=True)
