@@ -117,6 +117,25 @@ def decode_single_launch(n, k, T):
     return n <= 64 and n * k <= 1024
 
 
+def profiled_traffic(workload, kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu captures, or None
+    when there is none or the kernel's sources changed since it was taken."""
+    import hashlib
+
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    rec = json.load(open(path)).get(workload)
+    if not rec or rec.get("kernel") != kernel:
+        return None
+    csrc = os.path.join(ROOT, "nvfp4_quantized_moe_topk_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in (rec["source"], "common.cuh", "kernels.h"):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return float(rec["bytes_per_launch"]) if h.hexdigest()[:16] == rec["source_sha"] else None
+
+
 # ----------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = "index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active," \
@@ -359,6 +378,7 @@ def run_ours(args):
         achieved = b_alg / (per_launch_ms[dom] / 1000.0) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": None}
+    roof["traffic"] = profiled_traffic(args.workload, dom)
     roof["kernel"] = dom
     roof["kernel_ms"] = per_launch_ms[dom]
     roof["peak_source"] = peaks["source"]
