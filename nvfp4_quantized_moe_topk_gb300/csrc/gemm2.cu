@@ -19,12 +19,17 @@
 //               TMA tile of activations (192 rows x 64 bf16, 128-byte swizzle)
 //   warp 1      one thread issues tcgen05.mma.cta_group::1.kind::f16 with A
 //               in TMEM, B in shared memory, D in TMEM (two accumulators)
-//   warp 2      allocates / frees the 512 TMEM columns
+//   warp 2      allocates / frees the 512 TMEM columns; waits on the stage
+//               barriers for the issuer and hands each k-block over through a
+//               named barrier (the issuer must not read shared memory)
 //   warp 3      builds the tile list (experts above the threshold)
-//   warps 4-11  unpack: thread = (feature row, half of the k-block); 16 code
-//               bytes -> 16 bf16 pairs (bit placement + one bf16 multiply by
-//               the scale), tcgen05.st into the A stage of its TMEM lane
-//   warps 12-15 epilogue: tcgen05.ld, alpha, fp32 rows or bf16(relu^2) rows
+//   warps 4-19  unpack, in two groups of 8 taking alternate k-blocks: thread =
+//               (feature row, half of the k-block); 16 code bytes -> 16 bf16
+//               pairs (bit placement + one bf16 multiply by the scale),
+//               tcgen05.st into the A stage of its TMEM lane; a warp signals a
+//               stage ready only after unpacking its next k-block, so the
+//               store's latency hides behind that work
+//   warps 20-23 epilogue: tcgen05.ld, alpha, fp32 rows or bf16(relu^2) rows
 //
 // TMEM columns: accumulators [0,192) and [192,384), four 32-column A stages
 // from 384.  Tiles are (expert, 192 packed rows, 128 features), features
@@ -41,11 +46,12 @@ namespace g2 {
 constexpr int kM = 128;        // features per tile
 constexpr int kN = 192;        // packed rows (tokens) per tile
 constexpr int kK = 64;
-constexpr int kWStages = 4;    // packed weight blocks (shared memory)
-constexpr int kBStages = 4;    // activation tiles (shared memory)
+constexpr int kWStages = 8;    // packed weight blocks (shared memory)
+constexpr int kBStages = 7;    // activation tiles (shared memory): ~2.7k cycles of MMA work in flight
 constexpr int kAStages = 4;    // unpacked weights (tensor memory)
-constexpr int kThreads = 512;
-constexpr int kUnpackWarps = 8;
+constexpr int kUnpackWarps = 8;      // per group (one k-block: 4 row quarters x 2 halves)
+constexpr int kUnpackGroups = 2;
+constexpr int kThreads = 32 * (4 + kUnpackGroups * kUnpackWarps + 4);
 constexpr int kMaxGroups = 1024;
 constexpr uint32_t kWBytes = kGemmBlockBytes;     // 4608
 constexpr uint32_t kBBytes = kN * kK * 2;         // 24 KB
@@ -198,6 +204,18 @@ __device__ __forceinline__ bool g2_wait(uint64_t* bar, uint32_t parity, volatile
   }
 }
 
+// Warps 1 and 2 meet at named barrier 2; returns the OR of `abort` over both
+// (only warp 2 ever passes true).
+__device__ __forceinline__ bool g2_handoff(bool abort) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.or.pred p, 2, 64, q;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)abort)
+      : "memory");
+  return r != 0;
+}
+
 }  // namespace
 
 __global__ void __launch_bounds__(g2::kThreads, 1)
@@ -297,90 +315,133 @@ __global__ void __launch_bounds__(g2::kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    int ws = 0, bs = 0;
-    uint32_t wph = 0, bph = 0;
-    uint32_t w_out = 0, b_out = 0;  // stages whose last fill may still be landing
-    uint32_t w_iss[g2::kWStages] = {}, b_iss[g2::kBStages] = {};
-    bool ok = true;
-    for (int32_t t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
-      const G2Tile ti = g2_tile(t, tile_start, group_id, ngroups, a, nb);
-      const uint8_t* wsrc = a.blocks + ((size_t)ti.g * nb + ti.n0 / g2::kM) * KB * (size_t)g2::kWBytes;
-      for (int32_t kb = 0; kb < KB; ++kb) {
-        if (!g2_wait(&w_empty[ws], wph ^ 1u, abort_flag, a.err)) {
-          ok = false;
-          break;
-        }
-        if (lane == 0) {
+    // One thread: the waits of a full warp on already-completed barriers
+    // cost more than the copies they gate.
+    if (lane == 0) {
+      int ws = 0, bs = 0;
+      uint32_t wph = 0, bph = 0;
+      uint32_t w_out = 0, b_out = 0;  // stages whose last fill may still be landing
+      uint32_t w_iss[g2::kWStages] = {}, b_iss[g2::kBStages] = {};
+      bool ok = true;
+      for (int32_t t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+        const G2Tile ti = g2_tile(t, tile_start, group_id, ngroups, a, nb);
+        const uint8_t* wsrc = a.blocks + ((size_t)ti.g * nb + ti.n0 / g2::kM) * KB * (size_t)g2::kWBytes;
+        for (int32_t kb = 0; kb < KB; ++kb) {
+          if (!g2_wait(&w_empty[ws], wph ^ 1u, abort_flag, a.err)) {
+            ok = false;
+            break;
+          }
           mbar_arrive_expect_tx(&w_full[ws], g2::kWBytes);
           bulk_g2s(sm + g2::w + ws * g2::kWBytes, wsrc + (size_t)kb * g2::kWBytes, g2::kWBytes, &w_full[ws]);
-        }
-        w_out |= 1u << ws;
-        w_iss[ws] = wph;
-        if (++ws == g2::kWStages) {
-          ws = 0;
-          wph ^= 1u;
-        }
-        if (!g2_wait(&b_empty[bs], bph ^ 1u, abort_flag, a.err)) {
-          ok = false;
-          break;
-        }
-        if (lane == 0) {
+          w_out |= 1u << ws;
+          w_iss[ws] = wph;
+          if (++ws == g2::kWStages) {
+            ws = 0;
+            wph ^= 1u;
+          }
+          if (!g2_wait(&b_empty[bs], bph ^ 1u, abort_flag, a.err)) {
+            ok = false;
+            break;
+          }
           mbar_arrive_expect_tx(&b_full[bs], g2::kBBytes);
           tma_load_2d(sm + g2::b + bs * g2::kBBytes, &tmX, kb * g2::kK, ti.row0, &b_full[bs]);
+          b_out |= 1u << bs;
+          b_iss[bs] = bph;
+          if (++bs == g2::kBStages) {
+            bs = 0;
+            bph ^= 1u;
+          }
         }
-        b_out |= 1u << bs;
-        b_iss[bs] = bph;
-        if (++bs == g2::kBStages) {
-          bs = 0;
-          bph ^= 1u;
+      }
+      if (!ok) {
+        // Unwinding: let every copy issued here land before the CTA exits
+        // (bounded: 1 ms per stage).
+        for (int s = 0; s < g2::kWStages; ++s) {
+          if (!(w_out & (1u << s))) continue;
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(&w_full[s], w_iss[s]) && globaltimer_ns() - t0 < 1000000ull) {
+          }
+        }
+        for (int s = 0; s < g2::kBStages; ++s) {
+          if (!(b_out & (1u << s))) continue;
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(&b_full[s], b_iss[s]) && globaltimer_ns() - t0 < 1000000ull) {
+          }
         }
       }
     }
-    if (!ok) {
-      // Unwinding: let every copy this warp issued land before the CTA exits
-      // (bounded: 1 ms per stage).
-      for (int s = 0; s < g2::kWStages; ++s) {
-        if (!(w_out & (1u << s))) continue;
-        const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(&w_full[s], w_iss[s]) && globaltimer_ns() - t0 < 1000000ull) {
-        }
-      }
-      for (int s = 0; s < g2::kBStages; ++s) {
-        if (!(b_out & (1u << s))) continue;
-        const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(&b_full[s], b_iss[s]) && globaltimer_ns() - t0 < 1000000ull) {
-        }
-      }
-    }
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // A shared-memory load by the thread that issued tcgen05.mma waits until
+    // those MMAs have read their shared-memory operands, draining the tensor
+    // core's shallow queue; so this warp reads no shared memory per k-block.
+    // Warp 2 waits on the stage barriers and hands each k-block over through
+    // named barrier 2 (no memory access), with an abort bit riding along.
     int bs = 0, as = 0, it = 0;
-    uint32_t bph = 0, aph = 0;
-    bool ok = true;
-    for (int32_t t = blockIdx.x; t < total_tiles && ok; t += gridDim.x, ++it) {
-      const G2Tile ti = g2_tile(t, tile_start, group_id, ngroups, a, nb);
-      const uint32_t acc = it & 1, acc_phase = (it >> 1) & 1;
-      if (!g2_wait(&tmem_empty[acc], acc_phase ^ 1u, abort_flag, a.err)) break;
-      tc_fence_after();
+    bool done = false;
+    // descriptor of stage 0, k 0; the start-address field (address >> 4, low
+    // 14 bits) of the others is this plus the byte offset >> 4, no carry for
+    // offsets inside shared memory
+    const uint64_t bdesc0 = smem_desc_k128(smem_u32(sm + g2::b));
+    for (int32_t t = blockIdx.x; t < total_tiles && !done; t += gridDim.x, ++it) {
+      const G2Tile ti = g2_tile(t, tile_start, group_id, ngroups, a, nb);  // once per tile
+      const uint32_t acc = it & 1;
       const uint32_t ncols = (uint32_t)((ti.rows + 15) & ~15);
       const uint32_t idesc = idesc_bf16(g2::kM, ncols);
       const uint32_t d_tmem = tmem_base + acc * g2::kAccCols;
       for (int32_t kb = 0; kb < KB; ++kb) {
-        if (!g2_wait(&b_full[bs], bph, abort_flag, a.err) || !g2_wait(&a_full[as], aph, abort_flag, a.err)) {
-          ok = false;
+        if (g2_handoff(false)) {
+          done = true;
           break;
         }
-        tc_fence_after();
         if (lane == 0) {
-          const uint32_t b_base = smem_u32(sm + g2::b + bs * g2::kBBytes);
+          tc_fence_after();
+          const uint64_t bd = bdesc0 + (uint64_t)((uint32_t)(bs * g2::kBBytes) >> 4);
           const uint32_t a_tmem = tmem_base + g2::kACol0 + as * g2::kAStageCols;
+          tc_mma_bf16_ta(d_tmem, a_tmem, bd, idesc, kb != 0);
 #pragma unroll
-          for (int kk = 0; kk < g2::kK / 16; ++kk)
-            tc_mma_bf16_ta(d_tmem, a_tmem + kk * 8, smem_desc_k128(b_base + kk * 32), idesc, (kb | kk) != 0);
+          for (int kk = 1; kk < g2::kK / 16; ++kk) tc_mma_bf16_ta(d_tmem, a_tmem + kk * 8, bd + 2 * kk, idesc, 1);
           tc_commit(&b_empty[bs]);
           tc_commit(&a_empty[as]);
         }
+        if (++bs == g2::kBStages) bs = 0;
+        if (++as == g2::kAStages) as = 0;
+      }
+      if (done) break;
+      if (lane == 0) tc_commit(&tmem_full[acc]);
+      __syncwarp();
+    }
+    // all MMAs issued here have completed once `drain` flips
+    if (lane == 0) {
+      tc_commit(drain);
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(drain, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+      }
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ readiness
+    // For each k-block of the MMA issuer's sequence: the accumulator is free
+    // (first k-block of a tile), the activation tile and the unpacked weights
+    // have landed; then the hand-off.  Same trip count as the issuer.
+    int bs = 0, as = 0, it = 0;
+    uint32_t bph = 0, aph = 0;
+    bool done = false;
+    for (int32_t t = blockIdx.x; t < total_tiles && !done; t += gridDim.x, ++it) {
+      const uint32_t acc = it & 1, acc_phase = (it >> 1) & 1;
+      for (int32_t kb = 0; kb < KB; ++kb) {
+        bool fail = false;
+        if (lane == 0) {
+          if (kb == 0) fail = !g2_wait(&tmem_empty[acc], acc_phase ^ 1u, abort_flag, a.err);
+          fail = fail || !g2_wait(&b_full[bs], bph, abort_flag, a.err) ||
+                 !g2_wait(&a_full[as], aph, abort_flag, a.err);
+        }
         __syncwarp();
+        if (g2_handoff(fail)) {
+          done = true;
+          break;
+        }
         if (++bs == g2::kBStages) {
           bs = 0;
           bph ^= 1u;
@@ -390,68 +451,72 @@ __global__ void __launch_bounds__(g2::kThreads, 1)
           aph ^= 1u;
         }
       }
-      if (!ok) break;
-      if (lane == 0) tc_commit(&tmem_full[acc]);
-      __syncwarp();
     }
-    // all MMAs this thread issued have completed once `drain` flips
-    if (lane == 0) tc_commit(drain);
-    __syncwarp();
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(drain, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
-    }
-  } else if (warp >= 4 && warp < 4 + g2::kUnpackWarps) {
+  } else if (warp >= 4 && warp < 4 + g2::kUnpackGroups * g2::kUnpackWarps) {
     // ------------------------------------------------------------ unpack
-    const int q = warp & 3;                  // TMEM lanes 32q .. 32q+31
-    const int hf = (warp - 4) >> 2;          // k 32hf .. 32hf+31 of the block
+    // k-block L (counted over this CTA's tiles) uses weight stage L % 8
+    // (phase (L / 8) & 1) and A stage L % 4 (phase (L / 4) & 1); group L % 2
+    // unpacks it.
+    const int q = warp & 3;                        // TMEM lanes 32q .. 32q+31
+    const int hf = ((warp - 4) >> 2) & 1;          // k 32hf .. 32hf+31 of the block
+    const int grp = (warp - 4) >> 3;
     const int row = 32 * q + lane;
     const uint32_t col_off = ((uint32_t)(32 * q) << 16) + g2::kACol0 + hf * 16;
     const int cswap = (row >> 2) & 1;
-    int ws = 0, as = 0;
-    uint32_t wph = 0, aph = 0;
+    int prev = -1;  // A stage stored but not yet signalled
     bool ok = true;
+    int32_t L = 0;
     for (int32_t t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
-      for (int32_t kb = 0; kb < KB; ++kb) {
-        if (!g2_wait(&w_full[ws], wph, abort_flag, a.err) ||
-            !g2_wait(&a_empty[as], aph ^ 1u, abort_flag, a.err)) {
+      for (int32_t kb = 0; kb < KB; ++kb, ++L) {
+        if ((L & 1) != grp) continue;
+        static_assert(g2::kWStages == 8 && g2::kAStages == 4, "stage arithmetic below");
+        const int sw = L & 7, s = L & 3;
+        const uint32_t wph = (uint32_t)(L >> 3) & 1u, ph = (uint32_t)(L >> 2) & 1u;
+        if (!g2_wait(&w_full[sw], wph, abort_flag, a.err)) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        const uint8_t* wb = sm + g2::w + ws * g2::kWBytes;
+        const uint8_t* wb = sm + g2::w + sw * g2::kWBytes;
         const uint4 c = *reinterpret_cast<const uint4*>(wb + row * 32 + ((hf ^ cswap) << 4));
         const uint32_t sc = *reinterpret_cast<const uint16_t*>(wb + 4096 + row * 4 + 2 * hf);
         const uint32_t s0 = lut[sc & 0xFFu], s1 = lut[sc >> 8];
         __syncwarp();
-        if (lane == 0) mbar_arrive(&w_empty[ws]);  // release: the reads above are done
+        if (lane == 0) mbar_arrive(&w_empty[sw]);  // release: the reads above are done
         uint32_t r[16];
         const uint32_t words[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           uint32_t p0, p1, p2, p3;
           unpack_word(words[j], p0, p1, p2, p3);
-          const uint32_t s = j < 2 ? s0 : s1;
-          r[4 * j + 0] = mul_bf16x2(p0, s);
-          r[4 * j + 1] = mul_bf16x2(p1, s);
-          r[4 * j + 2] = mul_bf16x2(p2, s);
-          r[4 * j + 3] = mul_bf16x2(p3, s);
+          const uint32_t sv = j < 2 ? s0 : s1;
+          r[4 * j + 0] = mul_bf16x2(p0, sv);
+          r[4 * j + 1] = mul_bf16x2(p1, sv);
+          r[4 * j + 2] = mul_bf16x2(p2, sv);
+          r[4 * j + 3] = mul_bf16x2(p3, sv);
         }
-        tmem_st16(tmem_base + col_off + as * g2::kAStageCols, r);
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&a_full[as]);
-        if (++ws == g2::kWStages) {
-          ws = 0;
-          wph ^= 1u;
+        if (prev >= 0) {
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&a_full[prev]);
+          prev = -1;
         }
-        if (++as == g2::kAStages) {
-          as = 0;
-          aph ^= 1u;
+        if (!g2_wait(&a_empty[s], ph ^ 1u, abort_flag, a.err)) {
+          ok = false;
+          break;
         }
+        tc_fence_after();
+        tmem_st16(tmem_base + col_off + s * g2::kAStageCols, r);
+        prev = s;
       }
     }
-  } else if (warp >= 4 + g2::kUnpackWarps) {
+    if (prev >= 0) {
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&a_full[prev]);
+    }
+  } else if (warp >= 4 + g2::kUnpackGroups * g2::kUnpackWarps) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lanes 32q .. 32q+31: feature rows
     const int row = 32 * q + lane;
