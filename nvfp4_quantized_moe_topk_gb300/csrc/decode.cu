@@ -647,8 +647,12 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) decode_kernel(const __gr
     cx.advance(ci);
     ++issued;
   };
-  for (int32_t s = 0; s < P && ci.ph < 2; ++s) issue(s);
-  __syncwarp();
+  // Fill the rings in rounds -- every warp's first chunk, then every warp's
+  // second, ... -- so that the copies needed first lead the SM's copy queue.
+  for (int32_t s = 0; s < P; ++s) {
+    if (ci.ph < 2) issue(s);
+    all_warps_sync(nthreads);
+  }
 
   int32_t consumed = 0, slot = 0;
   uint32_t phase = 0;

@@ -188,13 +188,16 @@ __device__ __forceinline__ G2Tile g2_tile(int32_t t, const int32_t* tile_start, 
   return ti;
 }
 
-// Bounded wait that also gives up when another role has aborted.
+// Bounded wait that also gives up when another role has aborted.  Between
+// polls the thread is suspended (try_wait with a time hint) rather than
+// spinning: polling warps take shared-memory bandwidth from the MMA's operand
+// reads.
 __device__ __forceinline__ bool g2_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    for (int i = 0; i < 8; ++i)
+      if (mbar_try_wait_sleep(bar, parity, 1000u)) return true;
     if (*abort_flag) return false;
     if (globaltimer_ns() - t0 > kWaitLimitNs) {
       *abort_flag = 1;
