@@ -199,3 +199,33 @@ def test_n_zero_and_capacity(dev):
         layer.forward(x, to_dev(wl.topk_ids, dev), to_dev(wl.topk_weights, dev), dst, n_tokens=5)
     assert ei.value.status == 3
     layer.close()
+
+
+@pytest.mark.parametrize("name,single", [("decode-32", 0), ("tiny", -1)])
+def test_concurrent_streams_match_serial(dev, name, single):
+    """Two handles on two streams, enqueued back to back so they can overlap,
+    give the same bits as the same calls made one after the other."""
+    import torch
+
+    wl = W.generate(name)
+    routing2 = W.make_routing(wl.n, wl.E, wl.k, W.CONFIGS[name]["bias_sigma"], seed=4242)
+    layers = [make_layer(wl, dev, single_max_tokens=single) for _ in range(2)]
+    x = to_dev(wl.x, dev)
+    ids = [to_dev(wl.topk_ids, dev), to_dev(routing2[0], dev)]
+    tw = [to_dev(wl.topk_weights, dev), to_dev(routing2[1], dev)]
+    serial = []
+    for i in range(2):
+        d = to_dev(wl.dst, dev)
+        layers[i].forward(x, ids[i], tw[i], d)
+        torch.cuda.synchronize()
+        serial.append(bf16_from_dev(d))
+    streams = [torch.cuda.Stream(device=dev) for _ in range(2)]
+    dsts = [to_dev(wl.dst, dev) for _ in range(2)]
+    torch.cuda.synchronize()
+    for i in range(2):
+        layers[i].forward(x, ids[i], tw[i], dsts[i], stream=streams[i])
+    torch.cuda.synchronize()
+    for i in range(2):
+        assert np.array_equal(bf16_from_dev(dsts[i]), serial[i]), f"handle {i}"
+        assert layers[i].device_error() == 0
+        layers[i].close()
