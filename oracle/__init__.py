@@ -63,6 +63,8 @@ def _bind(L):
     L.or_weighted_row_sum.restype = _i64
     L.or_moe_forward.argtypes = [_i64, _int, _int, _int, _int] + [_ptr] * 13 + [_i64, _i64]
     L.or_moe_forward.restype = _int
+    L.or_router_topk.argtypes = [_ptr, _ptr, _i64, _int, _int, _ptr, _ptr, _ptr]
+    L.or_router_topk.restype = _int
     L.or_num_threads.argtypes = []
     L.or_num_threads.restype = _int
     return L
@@ -226,6 +228,20 @@ def moe_forward(wl, *, intermediates: bool = False, out_f64: bool = False,
     if rc != 0:
         raise ValueError(f"or_moe_forward failed ({rc})")
     return Result(dst, a_rows, y_rows, of)
+
+
+def router_topk(logits: np.ndarray, bias: np.ndarray | None, k: int):
+    """(ids int32 [n,k], weights fp32 [n,k], counts int32 [E]) of the router."""
+    logits = _c(logits, np.float32)
+    n, E = logits.shape
+    b = None if bias is None else _c(bias, np.float32)
+    ids = np.zeros((n, k), np.int32)
+    w = np.zeros((n, k), np.float32)
+    counts = np.zeros(E, np.int32)
+    rc = lib().or_router_topk(_p(logits), _p(b), n, E, k, _p(ids), _p(w), _p(counts))
+    if rc != 0:
+        raise ValueError(f"or_router_topk failed ({rc})")
+    return ids, w, counts
 
 
 def num_threads() -> int:

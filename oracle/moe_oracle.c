@@ -316,6 +316,56 @@ int or_moe_forward(int64_t n, int H, int I, int E, int k, const uint16_t *x, con
 }
 
 /* Number of OpenMP threads the oracle runs with (1 without OpenMP). */
+/* The router that produces the layer's input (the step before the path; the
+ * layer's synthetic workloads are routed this way: fp32 logits, an optional
+ * per-expert bias added to them, top-k, softmax renormalised over the k
+ * picked).  For each token t:
+ *   z[e]   = logits[t][e] + bias[e]          (one fp32 addition, bias may be NULL)
+ *   ids[t] = the k experts with the largest z in descending order, equal z
+ *            taken lower index first
+ *   w[t][j] = exp(z_j - z_0) / sum_i exp(z_i - z_0) over the k picked (fp64,
+ *            stored fp32)
+ *   counts[e] = number of tokens that picked e (if counts is not NULL)
+ * Selection is a plain scan per pick: the next pick is the best z among the
+ * experts after the previous pick in the order (z descending, index
+ * ascending).  Returns OR_ERR_ARG for k outside [1, E]. */
+int or_router_topk(const float *logits, const float *bias, int64_t n, int E, int k, int32_t *ids, float *w,
+                   int32_t *counts) {
+  if (n < 0 || E <= 0 || k < 1 || k > E) return OR_ERR_ARG;
+  if (counts)
+    for (int e = 0; e < E; ++e) counts[e] = 0;
+  double *zp = (double *)malloc(sizeof(double) * (size_t)k);
+  if (!zp) return OR_ERR_NOMEM;
+  for (int64_t t = 0; t < n; ++t) {
+    const float *row = logits + t * E;
+    float prev_z = 0.0f;
+    int prev_e = -1;
+    for (int j = 0; j < k; ++j) {
+      int best = -1;
+      float best_z = 0.0f;
+      for (int e = 0; e < E; ++e) {
+        const float z = bias ? row[e] + bias[e] : row[e];
+        /* only experts after the previous pick in the order (z desc, e asc) */
+        if (prev_e >= 0 && !(z < prev_z || (z == prev_z && e > prev_e))) continue;
+        if (best < 0 || z > best_z) {
+          best = e;
+          best_z = z;
+        }
+      }
+      ids[t * k + j] = best;
+      zp[j] = (double)best_z;
+      prev_z = best_z;
+      prev_e = best;
+      if (counts) counts[best] += 1;
+    }
+    double sum = 0.0;
+    for (int j = 0; j < k; ++j) sum += exp(zp[j] - zp[0]);
+    for (int j = 0; j < k; ++j) w[t * k + j] = (float)(exp(zp[j] - zp[0]) / sum);
+  }
+  free(zp);
+  return OR_OK;
+}
+
 int or_num_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();

@@ -74,6 +74,18 @@ MUTATIONS = [
      "          double r = h > 0.0 ? h : 0.0;\n          uint16_t ab",
      "          double r = h;\n          uint16_t ab",
      [pins.test_all_negative_preactivations_leave_dst_unchanged]),
+    ("router_ties_to_higher_index",
+     "        if (best < 0 || z > best_z) {",
+     "        if (best < 0 || z >= best_z) {",
+     [pins.test_router_hand_fixture_with_ties_and_bias]),
+    ("router_bias_ignored",
+     "        const float z = bias ? row[e] + bias[e] : row[e];",
+     "        const float z = row[e];",
+     [pins.test_router_hand_fixture_with_ties_and_bias]),
+    ("router_weights_not_normalised",
+     "    for (int j = 0; j < k; ++j) w[t * k + j] = (float)(exp(zp[j] - zp[0]) / sum);",
+     "    for (int j = 0; j < k; ++j) w[t * k + j] = (float)(exp(zp[j] - zp[0]));",
+     [pins.test_router_closed_forms]),
 ]
 
 

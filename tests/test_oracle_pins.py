@@ -354,3 +354,48 @@ def test_token_range_sample_matches_full_run():
     part = oracle.moe_forward(wl, tok_range=(3, 6))
     assert np.array_equal(part.dst[3:6], full.dst[3:6])
     assert np.array_equal(part.dst[:3], wl.dst[:3])
+
+
+# ----------------------------------------------------------------- router
+def _biased(logits, bias):
+    return logits if bias is None else (logits + bias[None, :]).astype(np.float32)
+
+
+@pytest.mark.parametrize("n,E,k,sigma,seed", [(200, 128, 8, 0.0, 1), (300, 128, 6, 1.5, 2), (64, 1024, 32, 2.0, 3),
+                                              (17, 8, 8, 0.0, 4), (5, 3, 1, 1.0, 5)])
+def test_router_matches_argsort_and_softmax(n, E, k, sigma, seed):
+    """Top-k equals numpy's stable argsort of the fp32 biased logits (descending,
+    ties to the lower index); weights equal scipy's softmax of the picked ones;
+    counts equal bincount."""
+    from scipy.special import softmax
+
+    rng = np.random.Generator(np.random.PCG64(seed))
+    logits = rng.standard_normal((n, E), dtype=np.float32)
+    bias = (rng.standard_normal(E, dtype=np.float32) * np.float32(sigma)) if sigma > 0 else None
+    ids, w, counts = oracle.router_topk(logits, bias, k)
+    z = _biased(logits, bias)
+    ref_ids = np.argsort(-z.astype(np.float64), axis=1, kind="stable")[:, :k]
+    assert np.array_equal(ids, ref_ids)
+    picked = np.take_along_axis(z.astype(np.float64), ref_ids, axis=1)
+    assert np.allclose(w, softmax(picked, axis=1), rtol=1e-6, atol=0)
+    assert np.array_equal(counts, np.bincount(ref_ids.ravel(), minlength=E))
+
+
+def test_router_hand_fixture_with_ties_and_bias():
+    g = json.load(open(os.path.join(GOLDEN, "router_hand.json")))
+    ids, w, counts = oracle.router_topk(np.array(g["logits"], np.float32), np.array(g["bias"], np.float32), g["k"])
+    assert ids.tolist() == g["ids"]
+    assert np.allclose(w, np.array(g["weights"]), rtol=1e-6, atol=0)
+    assert counts.tolist() == g["counts"]
+
+
+def test_router_closed_forms():
+    rng = np.random.Generator(np.random.PCG64(9))
+    logits = rng.standard_normal((50, 16), dtype=np.float32)
+    _, w1, _ = oracle.router_topk(logits, None, 1)
+    assert np.all(w1 == 1.0)  # a single pick gets the whole weight
+    _, w, _ = oracle.router_topk(logits, None, 5)
+    assert np.allclose(w.astype(np.float64).sum(axis=1), 1.0, atol=1e-6)
+    assert np.all(np.diff(w, axis=1) <= 0)  # descending logits give descending weights
+    with pytest.raises(ValueError):
+        oracle.router_topk(logits, None, 17)
