@@ -385,6 +385,33 @@ def run_ours(args):
     layer_bytes = sum(b for kname, (b, f) in work.items())
     layer_flops = sum(f for kname, (b, f) in work.items() if kname.startswith("gemm"))
 
+    # the router that produces the layer's routing (timed on its own, same shapes)
+    router = None
+    try:
+        rng = np.random.Generator(np.random.PCG64(77))
+        logits = torch.from_numpy(rng.standard_normal((wl.n, wl.E), dtype=np.float32)).to(dev)
+        rbias = (torch.from_numpy(rng.standard_normal(wl.E, dtype=np.float32)).to(dev) * cfg["bias_sigma"]
+                 if cfg["bias_sigma"] > 0 else None)
+        r_ids = torch.empty((wl.n, wl.k), dtype=torch.int32, device=dev)
+        r_w = torch.empty((wl.n, wl.k), dtype=torch.float32, device=dev)
+        r_counts = torch.empty(wl.E, dtype=torch.int32, device=dev)
+        r_ms = []
+        with torch.cuda.stream(stream):
+            for i in range(3 + max(args.steps, 10)):
+                flush.fill_(float(i))
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                api.router_topk(logits, rbias, r_ids, r_w, r_counts, stream=stream)
+                e1.record(stream)
+                r_ms.append((e0, e1))
+            torch.cuda.synchronize()
+        r_t = statistics.median(a.elapsed_time(b) for a, b in r_ms[3:])
+        r_bytes = wl.n * wl.E * 4 + wl.n * wl.k * 8 + wl.E * 4 * (2 if rbias is not None else 1)
+        router = {"ms": r_t, "bytes": r_bytes, "gbs": r_bytes / (r_t / 1000.0) / 1e9,
+                  "frac_hbm": r_bytes / (r_t / 1000.0) / 1e9 / peaks["hbm_gbs"]}
+    except Exception as exc:  # reported, not fatal: the layer line stands on its own
+        router = {"error": str(exc)[:200]}
+
     # end to end through the public host-buffer entry point
     xh = torch.from_numpy(wl.x.view(np.int16)).pin_memory()
     dh = torch.from_numpy(wl.dst.view(np.int16).copy()).pin_memory()
@@ -423,6 +450,7 @@ def run_ours(args):
                   "per_kernel_ms": per_launch_ms},
         "e2e": {"value": world * wl.n / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
+        "router": router,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
         "wall_s_timed_region": t_wall,

@@ -188,6 +188,26 @@ MOE_API moe_status moe_nvfp4_kernel_times(moe_nvfp4_t handle, const char **names
 MOE_API moe_status nvfp4_matmul(const uint16_t *A, const uint8_t *codes, const uint8_t *scales, float global, void *C,
                         int32_t M, int32_t N, int32_t K, int32_t epilogue, moe_stream_t stream);
 
+/* The router that produces the layer's topk_ids / topk_weights (the step
+ * before the layer; the layer's workloads are routed this way: fp32 logits,
+ * optionally plus a per-expert bias, top-k, softmax renormalised over the k
+ * picked).  For each token t:
+ *   z[e]            = logits[t][e] + bias[e]   (one fp32 addition; bias may be NULL)
+ *   topk_ids[t]     = the top_k experts by descending z, equal z lower index first
+ *   topk_weights[t] = exp(z_j - z_0) / sum_i exp(z_i - z_0) over the picks (fp32)
+ *   counts[e]       = tokens that picked e (optional, may be NULL; zeroed first)
+ *   logits device fp32 [n][n_experts], bias device fp32 [n_experts],
+ *   topk_ids device int32 [n][top_k], topk_weights device fp32 [n][top_k],
+ *   counts device int32 [n_experts].
+ * One warp per token; ids are exact (fp32 comparisons), weights run-to-run
+ * identical.  Enqueued on `stream`, no allocation.  NaN logits are outside
+ * the contract.  Errors: MOE_ERR_INVALID_ARG (n < 0, top_k outside
+ * [1, n_experts], null or misaligned pointer), MOE_ERR_UNSUPPORTED
+ * (top_k > 32 or n_experts > 1024), MOE_ERR_CUDA. */
+MOE_API moe_status moe_router_topk(const float *logits, const float *bias, int32_t n, int32_t n_experts,
+                                   int32_t top_k, int32_t *topk_ids, float *topk_weights, int32_t *counts,
+                                   moe_stream_t stream);
+
 /* Deterministic weighted row sum (pull request #91, "What changes",
  * WeightedRowSum):
  *   dst[i][c] = bf16_rne(dst[i][c] + sum_{j=0..k-1} w[i][j] * src[rows[i][j]][c])

@@ -24,7 +24,7 @@ DEVFLAG_TIMEOUT = 0x2
 ENTRY_POINTS = ("moe_nvfp4_status_string", "moe_nvfp4_create", "moe_nvfp4_destroy", "moe_nvfp4_forward",
                 "moe_nvfp4_forward_host", "moe_nvfp4_get_device_error", "moe_nvfp4_debug_routing",
                 "moe_nvfp4_debug_intermediates", "moe_nvfp4_set_timing", "moe_nvfp4_kernel_times",
-                "nvfp4_matmul", "weighted_row_sum", "moe_nvfp4_forward_noalloc")
+                "nvfp4_matmul", "weighted_row_sum", "moe_nvfp4_forward_noalloc", "moe_router_topk")
 
 _lock = threading.Lock()
 _lib = None
@@ -79,6 +79,7 @@ def load(build_if_missing: bool = False):
                                              ctypes.POINTER(i64), i32, ctypes.POINTER(i32)]
         L.nvfp4_matmul.argtypes = [vp, vp, vp, ctypes.c_float, vp, i32, i32, i32, i32, vp]
         L.weighted_row_sum.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, vp]
+        L.moe_router_topk.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp, vp]
         L.moe_nvfp4_forward_noalloc.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(Weights), vp, vp, vp, vp,
                                                 i32, vp]
         for name in ENTRY_POINTS:
@@ -192,6 +193,15 @@ def nvfp4_matmul(A, codes, scales, global_scale: float, C, epilogue: int, stream
     _check(load().nvfp4_matmul(_ptr(A), _ptr(codes), _ptr(scales), float(global_scale), _ptr(C), M, N, K,
                                epilogue, _stream(stream)), "nvfp4_matmul")
     return C
+
+
+def router_topk(logits, bias, topk_ids, topk_weights, counts=None, stream=None):
+    """moe_router_topk: fills topk_ids [n,k] / topk_weights [n,k] (and counts [E]) from logits [n,E]."""
+    n, E = logits.shape
+    k = topk_ids.shape[1]
+    _check(load().moe_router_topk(_ptr(logits), _ptr(bias), n, E, k, _ptr(topk_ids), _ptr(topk_weights),
+                                  _ptr(counts), _stream(stream)), "moe_router_topk")
+    return topk_ids, topk_weights
 
 
 def weighted_row_sum(dst, src, rows, w, stream=None):

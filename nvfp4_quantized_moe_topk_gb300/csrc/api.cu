@@ -530,6 +530,18 @@ moe_status nvfp4_matmul(const uint16_t* A, const uint8_t* codes, const uint8_t* 
   return cuda_status(launch_gemm(ta, tb, m, device_sms(dev), reinterpret_cast<cudaStream_t>(stream), false));
 }
 
+moe_status moe_router_topk(const float* logits, const float* bias, int32_t n, int32_t n_experts, int32_t top_k,
+                           int32_t* topk_ids, float* topk_weights, int32_t* counts, moe_stream_t stream) {
+  if (n < 0 || n_experts <= 0 || top_k < 1 || top_k > n_experts) return MOE_ERR_INVALID_ARG;
+  if (top_k > 32 || n_experts > 1024) return MOE_ERR_UNSUPPORTED;
+  if (n > 0 && (!logits || !topk_ids || !topk_weights)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(logits, 4) || !aligned(bias, 4) || !aligned(topk_ids, 4) || !aligned(topk_weights, 4) ||
+      !aligned(counts, 4))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_router(logits, bias, n, n_experts, top_k, topk_ids, topk_weights, counts,
+                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
 moe_status weighted_row_sum(uint16_t* dst, const float* src, const int32_t* rows, const float* w, int32_t n,
                             int32_t k, int32_t cols, int32_t src_rows, moe_stream_t stream) {
   if (n < 0 || k <= 0 || cols <= 0 || src_rows < 0) return MOE_ERR_INVALID_ARG;

@@ -12,6 +12,12 @@ size_t routing_smem_bytes(int E);
 cudaError_t launch_routing(const int32_t* ids, int32_t R, int32_t E, int32_t* counts, int32_t* offsets,
                            int32_t* perm_pair, int32_t* inv, int32_t* err, cudaStream_t s);
 
+// ------------------------------------------------------------------ router
+// ids/w [n][k] from fp32 logits [n][E] (+ bias [E] or nullptr); counts [E]
+// (or nullptr) is zeroed and receives the pick histogram.  k <= 32.
+cudaError_t launch_router(const float* logits, const float* bias, int32_t n, int32_t E, int32_t k, int32_t* ids,
+                          float* w, int32_t* counts, cudaStream_t s);
+
 // ------------------------------------------------------------ gather / combine
 // Xp[r][:] = x[perm_pair[r] / k][:] for r < offsets[E].
 cudaError_t launch_gather(const uint16_t* x, const int32_t* perm_pair, const int32_t* kept_rows, int32_t R,
