@@ -176,16 +176,19 @@ struct DecodeCtx {
   int32_t split;            // 1: each phase's k-tiles are cut evenly over the warps (one pass of <= 8 tokens)
   int32_t u_lo, n_up, d_lo, n_dn;  // this CTA's items per phase
   int32_t KTu, KTd, NTu, NTd;
+  int32_t pairs;            // 1: a work item is two consecutive row tiles, 0: one
+  int32_t NPu, NPd;         // work items per expert
+  uint32_t wbytes;          // weight bytes of a ring slot (the activation rows follow)
   int32_t Wu, Wd;           // warps that take part in each phase (split mode)
   int32_t ura, urb, dra, drb;      // this warp's tile range per phase (split mode)
 
   __device__ DecodeCtx(const DecodeArgs& args) : a(args) {}
 
   __device__ __forceinline__ void load_item(Cur& c) const {
-    const int32_t lo = c.ph ? d_lo : u_lo, NT = c.ph ? NTd : NTu;
+    const int32_t lo = c.ph ? d_lo : u_lo, NP = c.ph ? NPd : NPu;
     const int32_t flat = lo + c.i;
-    const int32_t ei = flat / NT;
-    c.rt = flat - ei * NT;
+    const int32_t ei = flat / NP;
+    c.rt = (flat - ei * NP) << pairs;  // first row tile of the item
     c.e = s_act[ei];
     c.cnt = s_counts[c.e];
     c.off = s_off[c.e];
@@ -251,13 +254,21 @@ struct DecodeCtx {
     return base + ((size_t)((size_t)c.e * NT + c.rt) * KT + c.kt) * kTileBytes;
   }
   __device__ __forceinline__ int32_t kts(const Cur& c) const { return min(kDecCK, c.kt_end - c.kt); }
-  // Lane 0 only: declare the chunk's bytes (weight tiles and activation rows,
-  // the latter possibly issued later) and bulk-copy the weight tiles.
+  __device__ __forceinline__ bool two(const Cur& c) const { return pairs && c.rt + 1 < (c.ph ? NTd : NTu); }
+  // Lane 0 only: declare the chunk's bytes (the k-tiles of both row tiles and
+  // the activation rows, the latter possibly issued later) and bulk-copy the
+  // weight tiles: row tile rt into the slot's first half, rt + 1 (the next
+  // KT tiles in memory) into the second.
   __device__ __forceinline__ void issue_weights(const Cur& c, uint8_t* slot, uint64_t* bar, uint64_t pol) const {
     const uint32_t n_kt = (uint32_t)kts(c);
     const uint32_t nt = (uint32_t)min(kDecPassTok, c.cnt - c.tok0);
-    mbar_arrive_expect_tx(bar, n_kt * (kTileBytes + nt * 128u));
-    bulk_g2s_hint(slot, chunk_src(c), n_kt * kTileBytes, bar, pol);
+    const bool pair = two(c);
+    mbar_arrive_expect_tx(bar, n_kt * ((pair ? 2u : 1u) * kTileBytes + nt * 128u));
+    const uint8_t* src = chunk_src(c);
+    bulk_g2s_hint(slot, src, n_kt * kTileBytes, bar, pol);
+    if (pair)
+      bulk_g2s_hint(slot + kDecCK * kTileBytes, src + (size_t)(c.ph ? KTd : KTu) * kTileBytes, n_kt * kTileBytes,
+                    bar, pol);
   }
   // Lanes g < nt: bulk-copy token column g's activation row segment (kts x 64
   // bf16) into the slot; it completes on the slot's barrier.
@@ -272,41 +283,47 @@ struct DecodeCtx {
       } else {
         src = a.Ap + (size_t)pr * a.I + c.kt * 64;
       }
-      bulk_g2s(slot + kDecCK * kTileBytes + lane * kDecActRow, src, (uint32_t)kts(c) * 128u, bar);
+      bulk_g2s(slot + wbytes + lane * kDecActRow, src, (uint32_t)kts(c) * 128u, bar);
     }
   }
 };
 
-// One chunk (up to kDecCK k-tiles of one 16-row tile) against the activation
-// rows staged in the same slot; `act` points at this lane's token column.
-__device__ __forceinline__ void chunk_mma(const uint8_t* wts, const uint8_t* act, int kts, int lane,
-                                          const uint32_t* scale_lut, float (&acc)[4], float (&acc2)[4]) {
+// One k-tile (16 rows x 64 k) of one row tile against this lane's activation
+// fragments x0 (k 16t .. 16t+7) and x1 (k 16t+8 .. 16t+15) of token column g.
+__device__ __forceinline__ void tile_mma(const uint8_t* tile, const uint4& x0, const uint4& x1, int lane,
+                                         const uint32_t* scale_lut, float (&acc)[4], float (&acc2)[4]) {
   const int g = lane >> 2, t = lane & 3;
+  const uint4 c = *reinterpret_cast<const uint4*>(tile + 16 * lane);
+  const uint32_t s0 = scale_lut[tile[512 + 4 * g + t]];
+  const uint32_t s1 = scale_lut[tile[512 + 4 * (g + 8) + t]];
+  uint32_t r0, r1, r2, r3;  // row g
+  uint32_t q0, q1, q2, q3;  // row g + 8
+  // word 0 of each row: k blocks 0 and 1 of the MMA
+  unpack_word(c.x, r0, r1, r2, r3);
+  unpack_word(c.z, q0, q1, q2, q3);
+  mma_bf16_16816(acc, mul_bf16x2(r0, s0), mul_bf16x2(q0, s1), mul_bf16x2(r1, s0), mul_bf16x2(q1, s1), x0.x, x0.y);
+  mma_bf16_16816(acc2, mul_bf16x2(r2, s0), mul_bf16x2(q2, s1), mul_bf16x2(r3, s0), mul_bf16x2(q3, s1), x0.z, x0.w);
+  // word 1 of each row: k blocks 2 and 3
+  unpack_word(c.y, r0, r1, r2, r3);
+  unpack_word(c.w, q0, q1, q2, q3);
+  mma_bf16_16816(acc, mul_bf16x2(r0, s0), mul_bf16x2(q0, s1), mul_bf16x2(r1, s0), mul_bf16x2(q1, s1), x1.x, x1.y);
+  mma_bf16_16816(acc2, mul_bf16x2(r2, s0), mul_bf16x2(q2, s1), mul_bf16x2(r3, s0), mul_bf16x2(q3, s1), x1.z, x1.w);
+}
+
+// One chunk: up to kDecCK k-tiles of a row-tile pair (the second only when
+// `pair`) against the activation rows staged in the same slot; `act` points at
+// this lane's token column.  The activation fragments of a k-tile serve both
+// row tiles.
+__device__ __forceinline__ void chunk_mma(const uint8_t* wts, const uint8_t* act, int kts, bool pair, int lane,
+                                          const uint32_t* scale_lut, float (&accA)[4], float (&accA2)[4],
+                                          float (&accB)[4], float (&accB2)[4]) {
 #pragma unroll
   for (int kt = 0; kt < kDecCK; ++kt) {
     if (kt < kts) {
-      const uint8_t* tile = wts + kt * kTileBytes;
-      const uint4 c = *reinterpret_cast<const uint4*>(tile + 16 * lane);
-      const uint32_t s0 = scale_lut[tile[512 + 4 * g + t]];
-      const uint32_t s1 = scale_lut[tile[512 + 4 * (g + 8) + t]];
       const uint4 x0 = *reinterpret_cast<const uint4*>(act + kt * 128);
       const uint4 x1 = *reinterpret_cast<const uint4*>(act + kt * 128 + 16);
-      uint32_t r0, r1, r2, r3;  // row g
-      uint32_t q0, q1, q2, q3;  // row g + 8
-      // word 0 of each row: k blocks 0 and 1 of the MMA
-      unpack_word(c.x, r0, r1, r2, r3);
-      unpack_word(c.z, q0, q1, q2, q3);
-      mma_bf16_16816(acc, mul_bf16x2(r0, s0), mul_bf16x2(q0, s1), mul_bf16x2(r1, s0), mul_bf16x2(q1, s1), x0.x,
-                     x0.y);
-      mma_bf16_16816(acc2, mul_bf16x2(r2, s0), mul_bf16x2(q2, s1), mul_bf16x2(r3, s0), mul_bf16x2(q3, s1), x0.z,
-                     x0.w);
-      // word 1 of each row: k blocks 2 and 3
-      unpack_word(c.y, r0, r1, r2, r3);
-      unpack_word(c.w, q0, q1, q2, q3);
-      mma_bf16_16816(acc, mul_bf16x2(r0, s0), mul_bf16x2(q0, s1), mul_bf16x2(r1, s0), mul_bf16x2(q1, s1), x1.x,
-                     x1.y);
-      mma_bf16_16816(acc2, mul_bf16x2(r2, s0), mul_bf16x2(q2, s1), mul_bf16x2(r3, s0), mul_bf16x2(q3, s1), x1.z,
-                     x1.w);
+      tile_mma(wts + kt * kTileBytes, x0, x1, lane, scale_lut, accA, accA2);
+      if (pair) tile_mma(wts + (kDecCK + kt) * kTileBytes, x0, x1, lane, scale_lut, accB, accB2);
     }
   }
 }
@@ -439,17 +456,18 @@ __device__ __forceinline__ void decode_grid_barrier(const DecodeArgs& a, int tid
   all_warps_sync(nthreads);
 }
 
-// The segment in `cur` is finished: if the warp holds only part of the tile's
-// k range, park the partial tile and let the last of the tile's warps sum all
-// parts in warp order; then apply alpha and store, and for a finished down
-// tile run the combine of its 16 columns if it was the last tile of them (for
-// batches of at most kDecLateCombine tokens; larger ones combine after a
-// second grid barrier).
-__device__ __forceinline__ void decode_epilogue(const DecodeCtx& cx, const Cur& cur, float (&v)[4], int lane,
+// The segment in `cur` is finished: if the warp holds only part of the
+// pair's k range, park its partial tiles and let the last of the pair's warps
+// sum all parts in warp order; then apply alpha and store both row tiles, and
+// for each finished down tile run the combine of its 16 columns if it was the
+// last tile of them (batches of at most kDecLateCombine tokens; larger ones
+// combine after a second grid barrier).
+__device__ __forceinline__ void decode_epilogue(const DecodeCtx& cx, const Cur& cur, float (&v)[8], int lane,
                                                 float4* partial, int32_t* pcount, const int32_t* s_inv,
                                                 int32_t n_act) {
   const DecodeArgs& a = cx.a;
   const int32_t up = cur.ph == 0;
+  const bool pair = cx.two(cur);
   if (cx.split) {
     const int32_t KT = up ? cx.KTu : cx.KTd;
     const int32_t ra = up ? cx.ura : cx.dra;
@@ -459,7 +477,9 @@ __device__ __forceinline__ void decode_epilogue(const DecodeCtx& cx, const Cur& 
       const int64_t TT = (int64_t)(up ? cx.n_up : cx.n_dn) * KT;
       const int64_t Wp = up ? cx.Wu : cx.Wd;
       const int32_t side = cur.i == first_item ? 0 : 1;
-      partial[(cx.warp * 2 + side) * 32 + lane] = make_float4(v[0], v[1], v[2], v[3]);
+      float4* slot = partial + ((cx.warp * 2 + side) * 32 + lane) * 2;
+      slot[0] = make_float4(v[0], v[1], v[2], v[3]);
+      slot[1] = make_float4(v[4], v[5], v[6], v[7]);
       __threadfence_block();
       __syncwarp();
       // warps holding tile rows i*KT .. (i+1)*KT-1 of this phase
@@ -473,24 +493,25 @@ __device__ __forceinline__ void decode_epilogue(const DecodeCtx& cx, const Cur& 
       last = __shfl_sync(0xffffffffu, last, 0);
       if (!last) return;
       __threadfence_block();
-      float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+      float4 rA = make_float4(0.f, 0.f, 0.f, 0.f), rB = rA;
       for (int32_t w2 = wf; w2 <= wl; ++w2) {
         const int32_t fi = (int32_t)((TT * w2) / Wp) / KT;
-        const float4 u = partial[(w2 * 2 + (cur.i == fi ? 0 : 1)) * 32 + lane];
-        r.x += u.x; r.y += u.y; r.z += u.z; r.w += u.w;
+        const float4* u = partial + ((w2 * 2 + (cur.i == fi ? 0 : 1)) * 32 + lane) * 2;
+        rA.x += u[0].x; rA.y += u[0].y; rA.z += u[0].z; rA.w += u[0].w;
+        rB.x += u[1].x; rB.y += u[1].y; rB.z += u[1].z; rB.w += u[1].w;
       }
-      v[0] = r.x; v[1] = r.y; v[2] = r.z; v[3] = r.w;
+      v[0] = rA.x; v[1] = rA.y; v[2] = rA.z; v[3] = rA.w;
+      v[4] = rB.x; v[5] = rB.y; v[6] = rB.z; v[7] = rB.w;
     }
   }
   const int g = lane >> 2, t = lane & 3;
   const float alpha = (up ? a.up_g : a.dn_g)[cur.e] * 256.0f;
   const int32_t nt = min(kDecPassTok, cur.cnt - cur.tok0);
-  const int32_t r0 = cur.rt * 16 + g;
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
+  for (int q = 0; q < 8; ++q) {
     const int32_t col = 2 * t + (q & 1);
-    const int32_t row = r0 + 8 * (q >> 1);
-    if (col < nt) {
+    const int32_t row = (cur.rt + (q >> 2)) * 16 + g + 8 * ((q >> 1) & 1);
+    if (col < nt && (q < 4 || pair)) {
       const size_t pr = (size_t)(cur.off + cur.tok0 + col);
       const float h = v[q] * alpha;
       if (up) {
@@ -502,26 +523,29 @@ __device__ __forceinline__ void decode_epilogue(const DecodeCtx& cx, const Cur& 
     }
   }
   if (up || a.ext || a.n > kDecLateCombine || cur.tok0 + kDecPassTok < cur.cnt) return;
-  // down tile complete: count it against its 16 columns
+  // down tiles complete: count each against its 16 columns
   __threadfence();
   __syncwarp();
-  int32_t last = 0;
-  if (lane == 0) {
-    last = atomicAdd(&a.col_done[cur.rt], 1) == n_act - 1;
-    if (last) a.col_done[cur.rt] = 0;
-  }
-  last = __shfl_sync(0xffffffffu, last, 0);
-  if (!last) return;
-  __threadfence();
-  const int32_t c = cur.rt * 16 + (lane & 15);
-  for (int32_t tk = lane >> 4; tk < a.n; tk += 2) {
-    uint16_t* d = a.dst + (size_t)tk * a.H + c;
-    float acc = __uint_as_float((uint32_t)*d << 16);
-    for (int32_t j = 0; j < a.k; ++j) {
-      const int32_t r = s_inv[tk * a.k + j];
-      if (r >= 0) acc = __fmaf_rn(a.tw[tk * a.k + j], ld_cg_f32(a.Yp + (size_t)r * a.H + c), acc);
+  for (int h = 0; h < (pair ? 2 : 1); ++h) {
+    const int32_t rt = cur.rt + h;
+    int32_t last = 0;
+    if (lane == 0) {
+      last = atomicAdd(&a.col_done[rt], 1) == n_act - 1;
+      if (last) a.col_done[rt] = 0;
     }
-    *d = f2bf_rn(acc);
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (!last) continue;
+    __threadfence();
+    const int32_t c = rt * 16 + (lane & 15);
+    for (int32_t tk = lane >> 4; tk < a.n; tk += 2) {
+      uint16_t* d = a.dst + (size_t)tk * a.H + c;
+      float acc = __uint_as_float((uint32_t)*d << 16);
+      for (int32_t j = 0; j < a.k; ++j) {
+        const int32_t r = s_inv[tk * a.k + j];
+        if (r >= 0) acc = __fmaf_rn(a.tw[tk * a.k + j], ld_cg_f32(a.Yp + (size_t)r * a.H + c), acc);
+      }
+      *d = f2bf_rn(acc);
+    }
   }
 }
 
@@ -597,7 +621,12 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) decode_kernel(const __gr
   const int32_t n_act = misc[1], cmax = misc[2];
   // slot size follows the widest token pass; keep at least two slots per warp
   const uint32_t nt_cap = (uint32_t)max(1, min(kDecPassTok, cmax));
-  const uint32_t slot_bytes = kDecCK * kTileBytes + nt_cap * kDecActRow;
+  // two row tiles per work item once an expert has several tokens (their
+  // activation fragments are then loaded once for both); single tiles keep
+  // the chunks small where the layer is all latency
+  const int32_t pairs = cmax >= 2;
+  const uint32_t wbytes = pairs ? kDecSlotBytes : kDecCK * kTileBytes;
+  const uint32_t slot_bytes = wbytes + nt_cap * kDecActRow;
   const uint32_t ring_bytes = L.total - L.ring;
   const int32_t Weff = max(1, min(W, (int32_t)(ring_bytes / (2u * slot_bytes))));
   const int32_t P = min(kDecMaxSlots, (int32_t)(ring_bytes / ((uint32_t)Weff * slot_bytes)));
@@ -606,9 +635,11 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) decode_kernel(const __gr
   cx.s_tok = s_tok; cx.s_counts = s_counts; cx.s_off = s_off; cx.s_act = s_act;
   cx.warp = warp; cx.W = Weff;
   cx.KTu = a.H / 64; cx.KTd = a.I / 64; cx.NTu = a.I / 16; cx.NTd = a.H / 16;
+  cx.pairs = pairs; cx.wbytes = wbytes;
+  cx.NPu = (cx.NTu + pairs) >> pairs; cx.NPd = (cx.NTd + pairs) >> pairs;
   {
     const int64_t G = gridDim.x, b = blockIdx.x;
-    const int64_t U = (int64_t)n_act * cx.NTu, D = (int64_t)n_act * cx.NTd;
+    const int64_t U = (int64_t)n_act * cx.NPu, D = (int64_t)n_act * cx.NPd;
     cx.u_lo = (int32_t)(U * b / G);
     cx.d_lo = (int32_t)(D * b / G);
     cx.n_up = (int32_t)(U * (b + 1) / G) - cx.u_lo;
@@ -656,7 +687,8 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) decode_kernel(const __gr
 
   int32_t consumed = 0, slot = 0;
   uint32_t phase = 0;
-  float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
+  float accA[4] = {0.f, 0.f, 0.f, 0.f}, accA2[4] = {0.f, 0.f, 0.f, 0.f};
+  float accB[4] = {0.f, 0.f, 0.f, 0.f}, accB2[4] = {0.f, 0.f, 0.f, 0.f};
   while (consumed < issued) {
     const Cur cur = wdesc[slot];
     if (cur.ph == 1 && !crossed) {
@@ -678,14 +710,17 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) decode_kernel(const __gr
       // once the first chunk has landed, ask L2 for the chunks past the ring
       Cur cp = ci;
       for (int q = 0; q < kDecL2Ahead && cp.ph < 2; ++q) {
-        prefetch_l2_bulk(cx.chunk_src(cp), (uint32_t)cx.kts(cp) * kTileBytes);
+        const uint8_t* src = cx.chunk_src(cp);
+        prefetch_l2_bulk(src, (uint32_t)cx.kts(cp) * kTileBytes);
+        if (cx.two(cp))
+          prefetch_l2_bulk(src + (size_t)(cp.ph ? cx.KTd : cx.KTu) * kTileBytes, (uint32_t)cx.kts(cp) * kTileBytes);
         cx.advance(cp);
       }
     }
     const uint8_t* sp = ring + (size_t)slot * slot_bytes;
     const int32_t nt = min(kDecPassTok, cur.cnt - cur.tok0);
-    const uint8_t* act = sp + kDecCK * kTileBytes + min(lane >> 2, nt - 1) * kDecActRow + (lane & 3) * 32;
-    chunk_mma(sp, act, cx.kts(cur), lane, lut, acc, acc2);
+    const uint8_t* act = sp + wbytes + min(lane >> 2, nt - 1) * kDecActRow + (lane & 3) * 32;
+    chunk_mma(sp, act, cx.kts(cur), cx.two(cur), lane, lut, accA, accA2, accB, accB2);
     ++consumed;
     __syncwarp();
     if (ci.ph < 2) {
@@ -698,12 +733,12 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) decode_kernel(const __gr
       phase ^= 1u;
     }
     if (cur.kt + kDecCK >= cur.kt_end) {
-      float v[4];
+      float v[8];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        v[q] = acc[q] + acc2[q];
-        acc[q] = 0.f;
-        acc2[q] = 0.f;
+        v[q] = accA[q] + accA2[q];
+        v[4 + q] = accB[q] + accB2[q];
+        accA[q] = accA2[q] = accB[q] = accB2[q] = 0.f;
       }
       decode_epilogue(cx, cur, v, lane, partial, pcount, s_inv, n_act);
     }

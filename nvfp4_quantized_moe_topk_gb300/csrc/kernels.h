@@ -91,7 +91,7 @@ constexpr int kTileBytes = 576;        // 16 rows x 64 k: 512 code bytes + 64 sc
 constexpr int kDecMaxWarps = 16;       // warps per CTA
 constexpr int kDecMaxSlots = 8;        // weight-ring slots per warp (at most)
 constexpr int kDecCK = 4;              // k-tiles (of 64) per chunk
-constexpr int kDecSlotBytes = kDecCK * kTileBytes;
+constexpr int kDecSlotBytes = 2 * kDecCK * kTileBytes;  // weights of a chunk: 2 row tiles x kDecCK k-tiles
 constexpr int kDecPassTok = 8;         // tokens per pass over a tile (one n8 MMA block)
 constexpr int kDecL2Ahead = 8;         // chunks past the ring requested into L2 at start
 constexpr int kDecLateCombine = 8;     // larger batches combine after a second grid barrier
@@ -122,7 +122,7 @@ inline DecLayout dec_layout(int32_t E, int32_t R, uint32_t budget) {
   L.act = take(4 * (uint32_t)E, 16);
   L.misc = take(64, 16);
   L.bars = take(8 * kDecMaxSlots * kDecMaxWarps, 16);
-  L.partial = take(2 * kDecMaxWarps * 32 * 16, 128);  // (warp, first/last segment) x lanes x float4
+  L.partial = take(2 * kDecMaxWarps * 32 * 32, 128);  // (warp, first/last segment) x lanes x 2 float4
   L.pcount = take(kDecMaxWarps * 4, 16);
   L.desc = take(kDecMaxWarps * kDecMaxSlots * 48, 16);  // per-slot chunk descriptors
   const uint32_t ring_at = (o + 127) / 128 * 128;
