@@ -9,7 +9,8 @@ workload, inputs already resident in HBM.  The default workload is decode-1
 with --workload.  Between timed steps a 256 MB write flushes the 129 MB L2 and
 the routing rotates over 8 seeded variants, so weights stream from HBM.  Each
 step is bracketed by CUDA events on the launching stream; the forward is
-replayed from a CUDA graph (--no-graph launches it directly).
+replayed from a CUDA graph or launched directly, whichever was faster over
+untimed probe steps (config.graph says which; --no-graph forces direct).
 
 Multi-GPU (torchrun): the layer does not shard across GPUs here, so every
 rank runs an independent replica on its own GPU (weak scaling, no data-path
@@ -340,6 +341,28 @@ def run_ours(args):
             graphs[i % N_ROUTINGS].replay()
         else:
             fwd(i)
+
+    if graphs is not None:
+        # A replayed one-kernel graph can cost more than the plain launch it
+        # holds: time both ways on untimed steps and keep the faster.
+        def probe():
+            evs = []
+            with torch.cuda.stream(stream):
+                for i in range(2 * N_ROUTINGS):
+                    flush.fill_(float(i))
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    step(i)
+                    e1.record(stream)
+                    evs.append((e0, e1))
+                torch.cuda.synchronize()
+            return statistics.median(a.elapsed_time(b) for a, b in evs)
+
+        t_graph = probe()
+        kept, graphs = graphs, None
+        t_direct = probe()
+        if t_graph < t_direct:
+            graphs = kept
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     with torch.cuda.stream(stream):
