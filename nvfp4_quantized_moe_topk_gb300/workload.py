@@ -22,6 +22,11 @@ order, from ``numpy.random.Generator(PCG64(seed))`` with
 7. down block-scale exponents: as 5, shape [E, H, I/16].
 8. ``dst`` (the pre-filled shared-expert output): fp32 N(0,1) [n, H] -> bf16.
 
+Gated (silu(gate) * up) workloads draw, after all of the above and from the
+same generator, 9. gate codes [E, I, H/2] and 10. gate scale exponents
+[E, I, H/16] as in 4 and 5, so the draws 1-8 are the same with or without a
+gate.
+
 Per-tensor globals are 2^-4 for every expert and matrix.  Top-k takes the k
 largest biased logits of each token (ties to the lower expert index) in
 descending order; the k routing weights are a softmax over those k biased
@@ -67,6 +72,13 @@ class Workload:
     up_global: np.ndarray  # float32 [E]
     down_global: np.ndarray  # float32 [E]
     dst: np.ndarray  # uint16 [n, H] (bf16 bit patterns), the pre-filled output
+    gate_codes: np.ndarray | None = None  # uint8 [E, I, H/2] (gated workloads only)
+    gate_scales: np.ndarray | None = None  # uint8 [E, I, H/16]
+    gate_global: np.ndarray | None = None  # float32 [E]
+
+    @property
+    def gated(self) -> bool:
+        return self.gate_codes is not None
 
     @property
     def R(self) -> int:
@@ -113,8 +125,16 @@ def make_routing(n: int, E: int, k: int, bias_sigma: float, seed: int) -> tuple[
     return route_topk(logits, k)
 
 
-def generate(name: str, seed: int | None = None, *, n: int | None = None, weights: bool = True) -> Workload:
-    """Draw the named workload.  ``n`` overrides the token count (same recipe)."""
+def _draw_gate(rng, E: int, H: int, I: int, lo: int = -4, hi: int = 2):
+    codes = rng.integers(0, 256, size=(E, I, H // 2), dtype=np.uint8)
+    scales = e4m3_byte_of_pow2(rng.integers(lo, hi + 1, size=(E, I, H // 16), dtype=np.int32))
+    return codes, scales, np.full(E, GLOBAL_SCALE, dtype=np.float32)
+
+
+def generate(name: str, seed: int | None = None, *, n: int | None = None, weights: bool = True,
+             gated: bool = False) -> Workload:
+    """Draw the named workload.  ``n`` overrides the token count (same recipe);
+    ``gated`` adds gate weights (drawn last)."""
     cfg = dict(CONFIGS[name])
     if n is not None:
         cfg["n"] = int(n)
@@ -137,12 +157,15 @@ def generate(name: str, seed: int | None = None, *, n: int | None = None, weight
         up_scales = down_codes = down_scales = up_codes
     dst = f32_to_bf16_bits(rng.standard_normal((n_, H), dtype=np.float32))
     g = np.full(E, GLOBAL_SCALE, dtype=np.float32)
-    return Workload(name, n_, H, I, E, k, x, ids, w, up_codes, up_scales, down_codes, down_scales,
-                    g.copy(), g.copy(), dst)
+    wl = Workload(name, n_, H, I, E, k, x, ids, w, up_codes, up_scales, down_codes, down_scales,
+                  g.copy(), g.copy(), dst)
+    if gated and weights:
+        wl.gate_codes, wl.gate_scales, wl.gate_global = _draw_gate(rng, E, H, I)
+    return wl
 
 
 def small_custom(n: int, H: int, I: int, E: int, k: int, seed: int, *, bias_sigma: float = 0.0,
-                 scale_exp=(-4, 2)) -> Workload:
+                 scale_exp=(-4, 2), gated: bool = False) -> Workload:
     """Same recipe at arbitrary (small) shapes, for parity and edge-case tests."""
     rng = np.random.Generator(np.random.PCG64(seed))
     x = f32_to_bf16_bits(rng.standard_normal((n, H), dtype=np.float32))
@@ -159,8 +182,11 @@ def small_custom(n: int, H: int, I: int, E: int, k: int, seed: int, *, bias_sigm
     down_scales = e4m3_byte_of_pow2(rng.integers(lo, hi + 1, size=(E, H, I // 16), dtype=np.int32))
     dst = f32_to_bf16_bits(rng.standard_normal((n, H), dtype=np.float32))
     g = np.full(E, GLOBAL_SCALE, dtype=np.float32)
-    return Workload("custom", n, H, I, E, k, x, ids, w, up_codes, up_scales, down_codes, down_scales,
-                    g.copy(), g.copy(), dst)
+    wl = Workload("custom", n, H, I, E, k, x, ids, w, up_codes, up_scales, down_codes, down_scales,
+                  g.copy(), g.copy(), dst)
+    if gated:
+        wl.gate_codes, wl.gate_scales, wl.gate_global = _draw_gate(rng, E, H, I, lo, hi)
+    return wl
 
 
 def expected_rows(name: str) -> int:
@@ -168,9 +194,10 @@ def expected_rows(name: str) -> int:
     return c["n"] * c["k"]
 
 
-def weight_bytes_per_expert(H: int, I: int) -> int:
-    """Packed NVFP4 bytes of one expert's up and down matrices (codes + block scales)."""
-    return 2 * (H * I // 2 + H * I // 16)
+def weight_bytes_per_expert(H: int, I: int, gated: bool = False) -> int:
+    """Packed NVFP4 bytes of one expert's matrices (codes + block scales): up and
+    down, plus the gate when gated."""
+    return (3 if gated else 2) * (H * I // 2 + H * I // 16)
 
 
 def l2_flush_bytes() -> int:

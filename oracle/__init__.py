@@ -63,6 +63,8 @@ def _bind(L):
     L.or_weighted_row_sum.restype = _i64
     L.or_moe_forward.argtypes = [_i64, _int, _int, _int, _int] + [_ptr] * 13 + [_i64, _i64]
     L.or_moe_forward.restype = _int
+    L.or_moe_forward_act.argtypes = [_i64, _int, _int, _int, _int] + [_ptr] * 9 + [_int] + [_ptr] * 7 + [_i64, _i64]
+    L.or_moe_forward_act.restype = _int
     L.or_router_topk.argtypes = [_ptr, _ptr, _i64, _int, _int, _ptr, _ptr, _ptr]
     L.or_router_topk.restype = _int
     L.or_num_threads.argtypes = []
@@ -210,7 +212,10 @@ class Result:
 
 def moe_forward(wl, *, intermediates: bool = False, out_f64: bool = False,
                 tok_range: tuple[int, int] | None = None) -> Result:
-    """Run the layer on a ``workload.Workload``; wl.dst is not modified."""
+    """Run the layer on a ``workload.Workload``; wl.dst is not modified.
+
+    A workload with gate weights (``wl.gate_codes`` not None) runs the gated
+    (silu(gate) * up) form, otherwise relu^2."""
     n, H, I, E, k = wl.n, wl.H, wl.I, wl.E, wl.k
     x = _c(wl.x, np.uint16)
     ids = _c(wl.topk_ids, np.int32)
@@ -223,8 +228,16 @@ def moe_forward(wl, *, intermediates: bool = False, out_f64: bool = False,
     y_rows = np.zeros((R, H), np.float64) if intermediates else None
     of = np.zeros((n, H), np.float64) if out_f64 else None
     t0, t1 = tok_range if tok_range is not None else (0, n)
-    rc = lib().or_moe_forward(n, H, I, E, k, _p(x), _p(ids), _p(w), *[_p(a) for a in arrs], _p(ug), _p(dg),
-                              _p(dst), _p(a_rows), _p(y_rows), _p(of), t0, t1)
+    gated = getattr(wl, "gate_codes", None) is not None
+    if gated:
+        gc, gs = _c(wl.gate_codes, np.uint8), _c(wl.gate_scales, np.uint8)
+        gg = _c(wl.gate_global, np.float32)
+        rc = lib().or_moe_forward_act(n, H, I, E, k, _p(x), _p(ids), _p(w), *[_p(a) for a in arrs], _p(ug),
+                                      _p(dg), 1, _p(gc), _p(gs), _p(gg), _p(dst), _p(a_rows), _p(y_rows), _p(of),
+                                      t0, t1)
+    else:
+        rc = lib().or_moe_forward(n, H, I, E, k, _p(x), _p(ids), _p(w), *[_p(a) for a in arrs], _p(ug), _p(dg),
+                                  _p(dst), _p(a_rows), _p(y_rows), _p(of), t0, t1)
     if rc != 0:
         raise ValueError(f"or_moe_forward failed ({rc})")
     return Result(dst, a_rows, y_rows, of)

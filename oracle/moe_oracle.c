@@ -18,7 +18,16 @@
  *     y_c = g_dn[e] * sum_i Wdn_e[c][i] * a_i                    (fp64)
  * and then
  *     out[t][c] = bf16_rne(dst[t][c] + sum_{j=0..k-1} w[t,j] * y^{(t,j)}_c)
- * with W[r][c] = e2m1(code) * e4m3(scale[r][c/16]) decoded exactly.  The
+ * with W[r][c] = e2m1(code) * e4m3(scale[r][c/16]) decoded exactly.
+ *
+ * The gated variant (the "gate-up" expert kernel of "nvfp4 experts cuda:
+ * decode kernels stall on load latency ... #2265", section "What ncu shows",
+ * whose warps read "both rows' inputs" per output) replaces the up step by
+ *     g_i = g_gate[e] * sum_c Wgate_e[i][c] * x[t][c]           (fp64)
+ *     u_i = g_up[e]   * sum_c Wup_e[i][c]   * x[t][c]           (fp64)
+ *     a_i = bf16_rne(silu(g_i) * u_i),  silu(g) = g / (1 + exp(-g))
+ * (the SwiGLU form of the models that page names; the page does not print the
+ * activation, so this is the reading taken).  The
  * gathering into packed rows only reorders this work, so the oracle computes
  * the routing (counts, offsets, stable permutation) separately, and uses it
  * only to report per-row intermediates in packed-row order.
@@ -229,19 +238,24 @@ int64_t or_weighted_row_sum(uint16_t *dst, const double *src, const int32_t *row
 /* ------------------------------------------------------ the whole layer */
 
 /* The MoE expert layer on the plain per-pair definition (see file header).
+ * act = 0: relu^2 (gate arrays unused, may be NULL); act = 1: the gated form,
+ * gate_codes/gate_scales [E][I][H/2], [E][I][H/16] and gate_global [E].
  * dst [n][H] bf16 is updated in place.  Optional outputs (NULL to skip), all
  * indexed by packed row r = inv[p] from or_routing on the same ids:
- *   a_rows   [R][I] bf16  the relu^2 intermediate of every kept pair
+ *   a_rows   [R][I] bf16  the intermediate (relu^2 or silu*up) of every kept pair
  *   y_rows   [R][H] fp64  the down-projection of every kept pair
  *   out_f64  [n][H] fp64  dst + sum_j w y before the final rounding
  * tok_begin/tok_end restrict the work to a token range (for bounded samples);
  * pass 0 and n for all tokens.  Returns 0, or < 0 on a bad argument / NaN scale. */
-int or_moe_forward(int64_t n, int H, int I, int E, int k, const uint16_t *x, const int32_t *ids,
-                   const float *topk_w, const uint8_t *up_codes, const uint8_t *up_scales,
-                   const uint8_t *dn_codes, const uint8_t *dn_scales, const float *up_global,
-                   const float *dn_global, uint16_t *dst, uint16_t *a_rows, double *y_rows,
-                   double *out_f64, int64_t tok_begin, int64_t tok_end) {
+int or_moe_forward_act(int64_t n, int H, int I, int E, int k, const uint16_t *x, const int32_t *ids,
+                       const float *topk_w, const uint8_t *up_codes, const uint8_t *up_scales,
+                       const uint8_t *dn_codes, const uint8_t *dn_scales, const float *up_global,
+                       const float *dn_global, int act, const uint8_t *gate_codes, const uint8_t *gate_scales,
+                       const float *gate_global, uint16_t *dst, uint16_t *a_rows, double *y_rows,
+                       double *out_f64, int64_t tok_begin, int64_t tok_end) {
   if (n < 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0 || H % 32 || I % 32) return OR_ERR_ARG;
+  if (act != 0 && act != 1) return OR_ERR_ARG;
+  if (act == 1 && (!gate_codes || !gate_scales || !gate_global)) return OR_ERR_ARG;
   if (tok_begin < 0 || tok_end > n || tok_begin > tok_end) return OR_ERR_ARG;
   int64_t R = n * (int64_t)k;
   int32_t *inv = NULL;
@@ -278,7 +292,7 @@ int or_moe_forward(int64_t n, int H, int I, int E, int k, const uint16_t *x, con
         const uint8_t *us = up_scales + (int64_t)e * (up_mat / 16);
         const uint8_t *dc = dn_codes + (int64_t)e * (up_mat / 2);
         const uint8_t *ds = dn_scales + (int64_t)e * (up_mat / 16);
-        /* up projection and relu^2, one bf16 rounding */
+        /* up projection and the activation, one bf16 rounding */
         for (int i = 0; i < I; ++i) {
           double h = 0.0, w;
           for (int c = 0; c < H; ++c) {
@@ -286,8 +300,22 @@ int or_moe_forward(int64_t n, int H, int I, int E, int k, const uint16_t *x, con
             h += w * xd[c];
           }
           h *= (double)up_global[e];
-          double r = h > 0.0 ? h : 0.0;
-          uint16_t ab = or_bf16_from_double(r * r);
+          double av;
+          if (act == 0) {
+            double r = h > 0.0 ? h : 0.0;
+            av = r * r;
+          } else {
+            const uint8_t *gc = gate_codes + (int64_t)e * (up_mat / 2);
+            const uint8_t *gs = gate_scales + (int64_t)e * (up_mat / 16);
+            double gv = 0.0;
+            for (int c = 0; c < H; ++c) {
+              if (weight_at(gc, gs, H, i, c, &w) != OR_OK) { bad = 1; w = 0.0; }
+              gv += w * xd[c];
+            }
+            gv *= (double)gate_global[e];
+            av = gv / (1.0 + exp(-gv)) * h;
+          }
+          uint16_t ab = or_bf16_from_double(av);
           a[i] = or_bf16_to_double(ab);
           if (a_rows) a_rows[(int64_t)inv[p] * I + i] = ab;
         }
@@ -315,7 +343,16 @@ int or_moe_forward(int64_t n, int H, int I, int E, int k, const uint16_t *x, con
   return bad ? OR_ERR_NAN : OR_OK;
 }
 
-/* Number of OpenMP threads the oracle runs with (1 without OpenMP). */
+/* The relu^2 layer (act = 0 of or_moe_forward_act). */
+int or_moe_forward(int64_t n, int H, int I, int E, int k, const uint16_t *x, const int32_t *ids,
+                   const float *topk_w, const uint8_t *up_codes, const uint8_t *up_scales,
+                   const uint8_t *dn_codes, const uint8_t *dn_scales, const float *up_global,
+                   const float *dn_global, uint16_t *dst, uint16_t *a_rows, double *y_rows,
+                   double *out_f64, int64_t tok_begin, int64_t tok_end) {
+  return or_moe_forward_act(n, H, I, E, k, x, ids, topk_w, up_codes, up_scales, dn_codes, dn_scales, up_global,
+                            dn_global, 0, NULL, NULL, NULL, dst, a_rows, y_rows, out_f64, tok_begin, tok_end);
+}
+
 /* The router that produces the layer's input (the step before the path; the
  * layer's synthetic workloads are routed this way: fp32 logits, an optional
  * per-expert bias added to them, top-k, softmax renormalised over the k
@@ -366,6 +403,7 @@ int or_router_topk(const float *logits, const float *bias, int64_t n, int E, int
   return OR_OK;
 }
 
+/* Number of OpenMP threads the oracle runs with (1 without OpenMP). */
 int or_num_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();

@@ -7,12 +7,14 @@ and a token that did not pick the expert weighs it zero.  Since gathering only
 skips work whose weight is zero, this form must agree with the C oracle's
 per-pair evaluation (up to fp64 summation order) -- the gather-vs-dense-masked
 pin.  Decoding uses independent sources: the e2m1 value table of the OCP
-Microscaling (MX) specification and torch's float8_e4m3fn conversion.
+Microscaling (MX) specification and torch's float8_e4m3fn conversion; the
+gated form's logistic function is scipy's ``expit``.
 """
 from __future__ import annotations
 
 import numpy as np
 import torch
+from scipy.special import expit
 
 # OCP MX specification, FP4 (E2M1) element values for codes 0..7; codes 8..15
 # are the same magnitudes with the sign bit set.
@@ -72,7 +74,8 @@ def moe_dense_masked(wl) -> dict:
     """Dense-masked layer: every expert over every token, weight 0 where unpicked.
 
     Returns the unrounded fp64 output, its bf16 rounding, and per-(token,
-    expert) relu^2 intermediates for the experts each token picked.
+    expert) intermediates (relu^2, or g * logistic(g) * u for a workload with
+    gate weights).
     """
     n, H, I, E, k = wl.n, wl.H, wl.I, wl.E, wl.k
     X = bf16_bits_to_f64(wl.x)
@@ -88,7 +91,12 @@ def moe_dense_masked(wl) -> dict:
         Wu = dequant(wl.up_codes[e], wl.up_scales[e])  # [I, H]
         Wd = dequant(wl.down_codes[e], wl.down_scales[e])  # [H, I]
         h = (X @ Wu.T) * float(wl.up_global[e])  # [n, I] over *all* tokens
-        a = bf16_round(np.maximum(h, 0.0) ** 2)
+        if getattr(wl, "gate_codes", None) is not None:
+            Wg = dequant(wl.gate_codes[e], wl.gate_scales[e])
+            gt = (X @ Wg.T) * float(wl.gate_global[e])
+            a = bf16_round(gt * expit(gt) * h)
+        else:
+            a = bf16_round(np.maximum(h, 0.0) ** 2)
         y = (a @ Wd.T) * float(wl.down_global[e])  # [n, H]
         out += mask_w[:, e:e + 1] * y
         a_all[e] = a

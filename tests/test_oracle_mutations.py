@@ -7,6 +7,7 @@ pin test to fail.  A pin set that lets any of these through is too weak.
 import pytest
 
 import oracle
+import test_oracle_gated as gated
 import test_oracle_pins as pins
 
 MUTATIONS = [
@@ -71,8 +72,8 @@ MUTATIONS = [
      "          h *= 1.0;",
      [lambda: pins.test_gather_equals_dense_masked(("tiny",))]),
     ("relu_dropped_in_layer",
-     "          double r = h > 0.0 ? h : 0.0;\n          uint16_t ab",
-     "          double r = h;\n          uint16_t ab",
+     "            double r = h > 0.0 ? h : 0.0;\n            av = r * r;",
+     "            double r = h;\n            av = r * r;",
      [pins.test_all_negative_preactivations_leave_dst_unchanged]),
     ("router_ties_to_higher_index",
      "        if (best < 0 || z > best_z) {",
@@ -86,6 +87,27 @@ MUTATIONS = [
      "    for (int j = 0; j < k; ++j) w[t * k + j] = (float)(exp(zp[j] - zp[0]) / sum);",
      "    for (int j = 0; j < k; ++j) w[t * k + j] = (float)(exp(zp[j] - zp[0]));",
      [pins.test_router_closed_forms]),
+    ("gate_and_up_swapped",
+     "av = gv / (1.0 + exp(-gv)) * h;",
+     "av = h / (1.0 + exp(-h)) * gv;",
+     [gated.test_large_positive_gate_passes_the_up_projection, gated.test_silu_odd_part_is_the_product]),
+    ("logistic_sign_flipped",
+     "av = gv / (1.0 + exp(-gv)) * h;",
+     "av = gv / (1.0 + exp(gv)) * h;",
+     [gated.test_logistic_points_from_fixture, gated.test_large_positive_gate_passes_the_up_projection]),
+    ("gelu_instead_of_silu",
+     "av = gv / (1.0 + exp(-gv)) * h;",
+     "av = gv * 0.5 * (1.0 + erf(gv / sqrt(2.0))) * h;",
+     [gated.test_logistic_points_from_fixture]),
+    ("gate_global_dropped",
+     "gv *= (double)gate_global[e];",
+     "gv *= 1.0;",
+     [gated.test_large_positive_gate_passes_the_up_projection]),
+    ("gate_reads_up_weights",
+     "if (weight_at(gc, gs, H, i, c, &w) != OR_OK)",
+     "if (weight_at(uc, us, H, i, c, &w) != OR_OK)",
+     [gated.test_large_positive_gate_passes_the_up_projection,
+      lambda: gated.test_gated_gather_equals_dense_masked((5, 64, 32, 4, 3, 51))]),
 ]
 
 
