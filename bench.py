@@ -52,6 +52,8 @@ def parse():
     p.add_argument("--gemv-max-rows", type=int, default=0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--gated", action="store_true",
+                   help="gated experts (silu(gate) * up) on the same workload shapes, gate weights drawn last")
     return p.parse_args()
 
 
@@ -76,6 +78,7 @@ def algorithmic_work(wl, ids_list, T):
     k fp32 rows per token read, ids/weights read.
     """
     H, I, E, k, n = wl.H, wl.I, wl.E, wl.k, wl.n
+    up_mats = 2 if wl.gated else 1  # a gated expert's up step reads the gate and the up matrix
     per = {"gemv_up": [0.0, 0.0], "gemv_down": [0.0, 0.0], "gemm_up": [0.0, 0.0], "gemm_down": [0.0, 0.0],
            "combine": [0.0, 0.0], "routing": [0.0, 0.0], "gather": [0.0, 0.0]}
     mat_bytes = H * I // 2 + H * I // 16
@@ -87,14 +90,14 @@ def algorithmic_work(wl, ids_list, T):
             if c[e] == 0:
                 continue
             if gemm_path and c[e] > T:
-                per["gemm_up"][1] += 2.0 * c[e] * I * H
+                per["gemm_up"][1] += 2.0 * c[e] * I * H * up_mats
                 per["gemm_down"][1] += 2.0 * c[e] * H * I
-                per["gemm_up"][0] += mat_bytes + c[e] * (H + I) * 2
+                per["gemm_up"][0] += up_mats * mat_bytes + c[e] * (H + I) * 2
                 per["gemm_down"][0] += mat_bytes + c[e] * (I * 2 + H * 4)
             else:
-                per["gemv_up"][0] += mat_bytes + c[e] * (H * 2 + I * 2)
+                per["gemv_up"][0] += up_mats * mat_bytes + c[e] * (H * 2 + I * 2)
                 per["gemv_down"][0] += mat_bytes + c[e] * (I * 2 + H * 4)
-                per["gemv_up"][1] += 2.0 * c[e] * I * H
+                per["gemv_up"][1] += 2.0 * c[e] * I * H * up_mats
                 per["gemv_down"][1] += 2.0 * c[e] * H * I
         per["combine"][0] += n * H * 2 * 2 + n * k * H * 4 + n * k * 8
         per["routing"][0] += n * k * 4 * 4
@@ -233,7 +236,7 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    wl = W.generate(args.workload)
+    wl = W.generate(args.workload, gated=args.gated)
     import oracle
 
     oracle.build()
@@ -253,7 +256,8 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * wall / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded)",
-            "config": {"workload": args.workload, "n": wl.n, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k},
+            "config": {"workload": args.workload, "n": wl.n, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
+                       "activation": "swiglu" if args.gated else "relu2"},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": samples[-1]["cores"], "kind": "oracle",
                              "sample": samples[-1]["sample"]},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -294,7 +298,7 @@ def run_ours(args):
     torch.cuda.set_device(dev)
     api.load(build_if_missing=True)
     cfg = W.CONFIGS[args.workload]
-    wl = W.generate(args.workload)
+    wl = W.generate(args.workload, gated=args.gated)
     T = args.gemv_max_rows if args.gemv_max_rows > 0 else 8
     routings = [(wl.topk_ids, wl.topk_weights)] + [
         W.make_routing(wl.n, wl.E, wl.k, cfg["bias_sigma"], seed=5000 + 97 * i) for i in range(1, N_ROUTINGS)]
@@ -305,8 +309,12 @@ def run_ours(args):
             a = a.view(np.int16)
         return torch.from_numpy(a).to(dev)
 
+    gate = {}
+    if wl.gated:
+        gate = dict(gate_codes=d(wl.gate_codes), gate_scales=d(wl.gate_scales), gate_global=d(wl.gate_global))
     layer = api.MoeLayer(wl.H, wl.I, wl.E, wl.k, wl.n, d(wl.up_codes), d(wl.up_scales), d(wl.down_codes),
-                         d(wl.down_scales), d(wl.up_global), d(wl.down_global), gemv_max_rows=args.gemv_max_rows)
+                         d(wl.down_scales), d(wl.up_global), d(wl.down_global), gemv_max_rows=args.gemv_max_rows,
+                         **gate)
     x = d(wl.x)
     dst = d(wl.dst)
     ids_d = [d(r[0]) for r in routings]
@@ -411,7 +419,7 @@ def run_ours(args):
         achieved = b_alg / (per_launch_ms[dom] / 1000.0) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": None}
-    roof["traffic"] = profiled_traffic(args.workload, dom)
+    roof["traffic"] = profiled_traffic(args.workload + ("+gated" if args.gated else ""), dom)
     roof["kernel"] = dom
     roof["kernel_ms"] = per_launch_ms[dom]
     roof["peak_source"] = peaks["source"]
@@ -473,7 +481,8 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, random NVFP4 weights)",
-        "config": {"workload": args.workload, "n": wl.n, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
+        "config": {"workload": args.workload, "activation": "swiglu" if args.gated else "relu2",
+                   "n": wl.n, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
                    "gemv_max_rows": T, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "flushed before every step (256 MB write)", "routings": N_ROUTINGS,
                    "graph": graphs is not None},

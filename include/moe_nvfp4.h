@@ -15,6 +15,14 @@
  *     y      = g_down[e] * (W_down[e] . a)                fp32 result
  *     dst[t] = bf16_rne(dst[t] + sum_{j=0..k-1} w[t][j] * y_(t,j))   j in order
  *
+ * Gated experts (config.activation = MOE_ACT_SWIGLU; the "gate-up" expert
+ * kernel of "nvfp4 experts cuda: decode kernels stall on load latency ...
+ * #2265", section "What ncu shows", whose output needs both a gate row and an
+ * up row; the activation is read as SwiGLU) replace the relu^2 step by
+ *
+ *     g      = g_gate[e] * (W_gate[e] . x[t])             fp32 accumulate
+ *     a      = bf16_rne(silu(g) * h),  silu(g) = g / (1 + exp(-g))
+ *
  * NVFP4 weights: W[r][c] = e2m1(code[r][c]) * e4m3(scale[r][c/16]); the
  * per-matrix fp32 global g is applied to the product (the GEMM alpha), never
  * folded into the bf16 weights (same page, bf16 NVFP4 GEMM).
@@ -29,6 +37,7 @@
  *   - Matrices are row-major.  Weights are [out][in] with K (= in) contiguous:
  *       up   codes [E][I][H/2]  scales [E][I][H/16]
  *       down codes [E][H][I/2]  scales [E][H][I/16]
+ *       gate codes [E][I][H/2]  scales [E][I][H/16]   (gated experts only)
  *     Code byte i of a row holds element 2i in its low nibble and element
  *     2i+1 in its high nibble.  Scale bytes are E4M3FN; NaN bytes (0x7F,
  *     0xFF) are outside the contract.
@@ -74,6 +83,10 @@ typedef void *moe_stream_t; /* a cudaStream_t */
 
 typedef struct moe_nvfp4 *moe_nvfp4_t;
 
+/* Expert activation (moe_nvfp4_config.activation). */
+#define MOE_ACT_RELU2 0  /* a = bf16(max(h, 0)^2) */
+#define MOE_ACT_SWIGLU 1 /* a = bf16(silu(g) * h), gate weights required */
+
 typedef struct moe_nvfp4_config {
   int32_t hidden;        /* H */
   int32_t inter;         /* I, the expert intermediate size */
@@ -89,6 +102,7 @@ typedef struct moe_nvfp4_config {
                             prefill) */
   int32_t single_max_tokens; /* batches with n <= this and n * k <= 1024 run
                                 as one launch; 0 selects 64, < 0 never */
+  int32_t activation;        /* MOE_ACT_RELU2 (0) or MOE_ACT_SWIGLU (1) */
 } moe_nvfp4_config;
 
 typedef struct moe_nvfp4_weights { /* device pointers, layouts as above */
@@ -98,6 +112,9 @@ typedef struct moe_nvfp4_weights { /* device pointers, layouts as above */
   const uint8_t *down_scales;
   const float *up_global;   /* [E] */
   const float *down_global; /* [E] */
+  const uint8_t *gate_codes;  /* MOE_ACT_SWIGLU: [E][I][H/2]; otherwise ignored (may be NULL) */
+  const uint8_t *gate_scales; /* MOE_ACT_SWIGLU: [E][I][H/16] */
+  const float *gate_global;   /* MOE_ACT_SWIGLU: [E] */
 } moe_nvfp4_weights;
 
 /* Human-readable name of a status (static storage, never NULL). */
@@ -109,8 +126,10 @@ MOE_API const char *moe_nvfp4_status_string(moe_status status);
  * max_tokens, so that forward never allocates (pull request #91, "Results",
  * names per-op cudaMalloc/cudaFree as the remaining host cost).  Work is
  * enqueued on `stream`, which is synchronized before returning.
- * Errors: MOE_ERR_INVALID_ARG (null pointer, max_tokens < 0),
- * MOE_ERR_UNSUPPORTED (shape), MOE_ERR_NO_DEVICE, MOE_ERR_CUDA (allocation).
+ * Errors: MOE_ERR_INVALID_ARG (null pointer -- the gate arrays too when
+ * activation is MOE_ACT_SWIGLU --, max_tokens < 0, activation not one of the
+ * MOE_ACT_ values), MOE_ERR_UNSUPPORTED (shape), MOE_ERR_NO_DEVICE,
+ * MOE_ERR_CUDA (allocation).
  * On error *out is set to NULL and nothing stays allocated. */
 MOE_API moe_status moe_nvfp4_create(const moe_nvfp4_config *config, const moe_nvfp4_weights *weights,
                             moe_stream_t stream, moe_nvfp4_t *out);

@@ -39,12 +39,16 @@ class MoeError(RuntimeError):
 class Config(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int32), ("inter", ctypes.c_int32), ("n_experts", ctypes.c_int32),
                 ("top_k", ctypes.c_int32), ("max_tokens", ctypes.c_int32), ("gemv_max_rows", ctypes.c_int32),
-                ("single_max_tokens", ctypes.c_int32)]
+                ("single_max_tokens", ctypes.c_int32), ("activation", ctypes.c_int32)]
+
+
+ACT_RELU2, ACT_SWIGLU = 0, 1
 
 
 class Weights(ctypes.Structure):
     _fields_ = [("up_codes", ctypes.c_void_p), ("up_scales", ctypes.c_void_p), ("down_codes", ctypes.c_void_p),
-                ("down_scales", ctypes.c_void_p), ("up_global", ctypes.c_void_p), ("down_global", ctypes.c_void_p)]
+                ("down_scales", ctypes.c_void_p), ("up_global", ctypes.c_void_p), ("down_global", ctypes.c_void_p),
+                ("gate_codes", ctypes.c_void_p), ("gate_scales", ctypes.c_void_p), ("gate_global", ctypes.c_void_p)]
 
 
 def library_path() -> str:
@@ -118,16 +122,22 @@ def _stream(stream):
 
 
 class MoeLayer:
-    """A created layer (``moe_nvfp4_create``); weights are copied into the handle."""
+    """A created layer (``moe_nvfp4_create``); weights are copied into the handle.
+
+    Passing gate weights (``gate_codes``, ``gate_scales``, ``gate_global``)
+    makes the experts gated: a = bf16(silu(gate) * up) instead of relu^2."""
 
     def __init__(self, hidden, inter, n_experts, top_k, max_tokens, up_codes, up_scales, down_codes, down_scales,
-                 up_global, down_global, gemv_max_rows: int = 0, single_max_tokens: int = 0, stream=None):
+                 up_global, down_global, gemv_max_rows: int = 0, single_max_tokens: int = 0, stream=None,
+                 gate_codes=None, gate_scales=None, gate_global=None):
         L = load()
         self.hidden, self.inter, self.n_experts, self.top_k = hidden, inter, n_experts, top_k
         self.max_tokens = max_tokens
-        cfg = Config(hidden, inter, n_experts, top_k, max_tokens, gemv_max_rows, single_max_tokens)
+        self.gated = gate_codes is not None
+        cfg = Config(hidden, inter, n_experts, top_k, max_tokens, gemv_max_rows, single_max_tokens,
+                     ACT_SWIGLU if self.gated else ACT_RELU2)
         w = Weights(_ptr(up_codes), _ptr(up_scales), _ptr(down_codes), _ptr(down_scales), _ptr(up_global),
-                    _ptr(down_global))
+                    _ptr(down_global), _ptr(gate_codes), _ptr(gate_scales), _ptr(gate_global))
         h = ctypes.c_void_p()
         _check(L.moe_nvfp4_create(ctypes.byref(cfg), ctypes.byref(w), _stream(stream), ctypes.byref(h)),
                "moe_nvfp4_create")
@@ -213,14 +223,15 @@ def weighted_row_sum(dst, src, rows, w, stream=None):
 
 
 def forward_noalloc(hidden, inter, n_experts, top_k, up_codes, up_scales, down_codes, down_scales, up_global,
-                    down_global, x, topk_ids, topk_weights, dst, n_tokens: int | None = None, stream=None):
+                    down_global, x, topk_ids, topk_weights, dst, n_tokens: int | None = None, stream=None,
+                    gate_codes=None, gate_scales=None, gate_global=None):
     """``moe_nvfp4_forward_noalloc``: the layer without a handle and without any
     device allocation (weights read in place; intermediates in the library's
-    fixed device array)."""
+    fixed device array).  Gate weights make the experts gated."""
     n = x.shape[0] if n_tokens is None else n_tokens
-    cfg = Config(hidden, inter, n_experts, top_k, n, 0)
+    cfg = Config(hidden, inter, n_experts, top_k, n, 0, 0, ACT_SWIGLU if gate_codes is not None else ACT_RELU2)
     w = Weights(_ptr(up_codes), _ptr(up_scales), _ptr(down_codes), _ptr(down_scales), _ptr(up_global),
-                _ptr(down_global))
+                _ptr(down_global), _ptr(gate_codes), _ptr(gate_scales), _ptr(gate_global))
     _check(load().moe_nvfp4_forward_noalloc(ctypes.byref(cfg), ctypes.byref(w), _ptr(x), _ptr(topk_ids),
                                             _ptr(topk_weights), _ptr(dst), n, _stream(stream)),
            "moe_nvfp4_forward_noalloc")

@@ -13,6 +13,12 @@
 //   T rows (both projections) -> tcgen05 grouped GEMM up -> grouped GEMM down
 //   -> WeightedRowSum
 //
+// Gated experts (silu(gate) * up): create interleaves the gate and up
+// matrices in groups of 16 rows (16 gate rows, then the 16 up rows of the
+// same features) into one 2I-row matrix and repacks that for both kernels, so
+// a streaming-kernel work item is a (gate, up) tile pair and a grouped-GEMM
+// weight block holds 64 features' gate and up rows.
+//
 // chained with programmatic dependent launch so each kernel's prologue
 // overlaps its predecessor's tail.  The GEMM kernels are enqueued only when
 // some expert can exceed the threshold T (n > T); which experts take which
@@ -59,6 +65,9 @@ struct moe_nvfp4 {
   // library-owned weights
   uint8_t *up_codes = nullptr, *up_scales = nullptr, *dn_codes = nullptr, *dn_scales = nullptr;
   float *up_g = nullptr, *dn_g = nullptr;
+  bool gated = false;
+  uint8_t *gate_codes = nullptr, *gate_scales = nullptr;
+  float* gate_g = nullptr;
   // the same weights in fragment-tile order for the single-launch small-batch path
   uint8_t *up_tiles = nullptr, *dn_tiles = nullptr;
   // and in packed 128-row blocks for the grouped GEMM
@@ -90,7 +99,8 @@ void free_handle(moe_nvfp4* h) {
   void* ptrs[] = {h->up_codes, h->up_scales, h->dn_codes, h->dn_scales, h->up_g,      h->dn_g,
                   h->counts,   h->offsets,   h->perm_pair, h->inv,      h->err,       h->Xp,
                   h->Ap,       h->Yp,        h->x_stage,   h->dst_stage, h->ids_stage, h->w_stage,
-                  h->up_tiles, h->dn_tiles,  h->col_done,  h->grid_bar,  h->up_blocks, h->dn_blocks};
+                  h->up_tiles, h->dn_tiles,  h->col_done,  h->grid_bar,  h->up_blocks, h->dn_blocks,
+                  h->gate_codes, h->gate_scales, h->gate_g};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   for (auto& s : h->slots) {
@@ -172,6 +182,9 @@ moe_status moe_nvfp4_create(const moe_nvfp4_config* config, const moe_nvfp4_weig
   if (!w->up_codes || !w->up_scales || !w->down_codes || !w->down_scales || !w->up_global || !w->down_global)
     return MOE_ERR_INVALID_ARG;
   const moe_nvfp4_config c = *config;
+  if (c.activation != MOE_ACT_RELU2 && c.activation != MOE_ACT_SWIGLU) return MOE_ERR_INVALID_ARG;
+  const bool gated = c.activation == MOE_ACT_SWIGLU;
+  if (gated && (!w->gate_codes || !w->gate_scales || !w->gate_global)) return MOE_ERR_INVALID_ARG;
   moe_status st = check_shape(c.hidden, c.inter, c.n_experts, c.top_k);
   if (st != MOE_OK) return st;
   if (c.max_tokens < 0) return MOE_ERR_INVALID_ARG;
@@ -189,8 +202,11 @@ moe_status moe_nvfp4_create(const moe_nvfp4_config* config, const moe_nvfp4_weig
   const size_t H = c.hidden, I = c.inter, E = c.n_experts;
   const size_t R = (size_t)c.max_tokens * c.top_k, Rr = R > 0 ? R : 1;
   const size_t mat_codes = E * H * I / 2, mat_scales = E * H * I / 16;
+  const size_t up_rows = gated ? 2 * I : I;  // rows of the (fused) up matrix the kernels stream
+  uint8_t* gu = nullptr;                     // gated: gate and up interleaved by 16 rows, [E][2I][H/2 + H/16]
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
+  h->gated = gated;
 #define TRY(x)                  \
   do {                          \
     e = (x);                    \
@@ -214,9 +230,9 @@ moe_status moe_nvfp4_create(const moe_nvfp4_config* config, const moe_nvfp4_weig
   TRY(cudaMalloc(&h->dst_stage, (size_t)(c.max_tokens > 0 ? c.max_tokens : 1) * H * 2));
   TRY(cudaMalloc(&h->ids_stage, Rr * sizeof(int32_t)));
   TRY(cudaMalloc(&h->w_stage, Rr * sizeof(float)));
-  TRY(cudaMalloc(&h->up_tiles, mat_codes + mat_scales));
+  TRY(cudaMalloc(&h->up_tiles, (mat_codes + mat_scales) * (gated ? 2 : 1)));
   TRY(cudaMalloc(&h->dn_tiles, mat_codes + mat_scales));
-  TRY(cudaMalloc(&h->up_blocks, gemm_blocks_bytes((int32_t)E, (int32_t)I, (int32_t)H)));
+  TRY(cudaMalloc(&h->up_blocks, gemm_blocks_bytes((int32_t)E, (int32_t)up_rows, (int32_t)H)));
   TRY(cudaMalloc(&h->dn_blocks, gemm_blocks_bytes((int32_t)E, (int32_t)H, (int32_t)I)));
   TRY(cudaMalloc(&h->col_done, (H / 16) * sizeof(int32_t)));
   TRY(cudaMalloc(&h->grid_bar, 2 * sizeof(int32_t)));
@@ -233,18 +249,41 @@ moe_status moe_nvfp4_create(const moe_nvfp4_config* config, const moe_nvfp4_weig
   TRY(cudaMemsetAsync(h->Yp, 0, Rr * H * 4, s));
   TRY(cudaMemsetAsync(h->col_done, 0, (H / 16) * sizeof(int32_t), s));
   TRY(cudaMemsetAsync(h->grid_bar, 0, 2 * sizeof(int32_t), s));
-  TRY(launch_repack_frag(h->up_codes, h->up_scales, (int32_t)E, (int32_t)I, (int32_t)H, h->up_tiles, s));
+  if (gated) {
+    TRY(cudaMalloc(&h->gate_codes, mat_codes));
+    TRY(cudaMalloc(&h->gate_scales, mat_scales));
+    TRY(cudaMalloc(&h->gate_g, E * sizeof(float)));
+    TRY(cudaMemcpyAsync(h->gate_codes, w->gate_codes, mat_codes, cudaMemcpyDeviceToDevice, s));
+    TRY(cudaMemcpyAsync(h->gate_scales, w->gate_scales, mat_scales, cudaMemcpyDeviceToDevice, s));
+    TRY(cudaMemcpyAsync(h->gate_g, w->gate_global, E * sizeof(float), cudaMemcpyDeviceToDevice, s));
+    // 16-row groups: [gate rows 16j..16j+15][up rows 16j..16j+15], codes then scales
+    TRY(cudaMalloc(&gu, 2 * (mat_codes + mat_scales)));
+    uint8_t* gu_codes = gu;
+    uint8_t* gu_scales = gu + 2 * mat_codes;
+    const size_t cblk = 16 * H / 2, sblk = 16 * H / 16, groups = E * I / 16;
+    TRY(cudaMemcpy2DAsync(gu_codes, 2 * cblk, h->gate_codes, cblk, cblk, groups, cudaMemcpyDeviceToDevice, s));
+    TRY(cudaMemcpy2DAsync(gu_codes + cblk, 2 * cblk, h->up_codes, cblk, cblk, groups, cudaMemcpyDeviceToDevice, s));
+    TRY(cudaMemcpy2DAsync(gu_scales, 2 * sblk, h->gate_scales, sblk, sblk, groups, cudaMemcpyDeviceToDevice, s));
+    TRY(cudaMemcpy2DAsync(gu_scales + sblk, 2 * sblk, h->up_scales, sblk, sblk, groups, cudaMemcpyDeviceToDevice,
+                          s));
+    TRY(launch_repack_frag(gu_codes, gu_scales, (int32_t)E, (int32_t)up_rows, (int32_t)H, h->up_tiles, s));
+    TRY(launch_repack_gemm(gu_codes, gu_scales, (int32_t)E, (int32_t)up_rows, (int32_t)H, h->up_blocks, s));
+  } else {
+    TRY(launch_repack_frag(h->up_codes, h->up_scales, (int32_t)E, (int32_t)I, (int32_t)H, h->up_tiles, s));
+    TRY(launch_repack_gemm(h->up_codes, h->up_scales, (int32_t)E, (int32_t)I, (int32_t)H, h->up_blocks, s));
+  }
   TRY(launch_repack_frag(h->dn_codes, h->dn_scales, (int32_t)E, (int32_t)H, (int32_t)I, h->dn_tiles, s));
-  TRY(launch_repack_gemm(h->up_codes, h->up_scales, (int32_t)E, (int32_t)I, (int32_t)H, h->up_blocks, s));
   TRY(launch_repack_gemm(h->dn_codes, h->dn_scales, (int32_t)E, (int32_t)H, (int32_t)I, h->dn_blocks, s));
   TRY(make_tmap_act_rows(&h->tm_xp, h->Xp, Rr, H, 192));
   TRY(make_tmap_act_rows(&h->tm_ap, h->Ap, Rr, I, 192));
   TRY(cudaStreamSynchronize(s));
 #undef TRY
+  if (gu) cudaFree(gu);
   *out = h;
   return MOE_OK;
 fail:
   cudaStreamSynchronize(s);
+  if (gu) cudaFree(gu);
   free_handle(h);
   return MOE_ERR_CUDA;
 }
@@ -270,6 +309,8 @@ static moe_status forward_impl(moe_nvfp4* h, const uint16_t* x, const int32_t* i
   d.dn_tiles = h->dn_tiles;
   d.up_g = h->up_g;
   d.dn_g = h->dn_g;
+  d.gate_g = h->gate_g;
+  d.gated = h->gated ? 1 : 0;
   d.x = x;
   d.ids = ids;
   d.tw = tw;
@@ -339,7 +380,13 @@ static moe_status forward_impl(moe_nvfp4* h, const uint16_t* x, const int32_t* i
     g.K = H;
     g.token_indexed = 1;
     g.relu2_bf16_out = 1;
+    g.gate_codes = h->gate_codes;
+    g.gate_scales = h->gate_scales;
+    g.gate_global = h->gate_g;
     e = launch_gemv(g, s, pdl);
+    g.gate_codes = nullptr;
+    g.gate_scales = nullptr;
+    g.gate_global = nullptr;
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
   Gemm2Args m{};
@@ -352,10 +399,11 @@ static moe_status forward_impl(moe_nvfp4* h, const uint16_t* x, const int32_t* i
     TimedLaunch tl(h, s, kKGemmUp);
     m.blocks = h->up_blocks;
     m.global = h->up_g;
-    m.N = I;
+    m.N = h->gated ? 2 * I : I;
     m.K = H;
     m.out = h->Ap;
-    m.epilogue = 1;
+    m.epilogue = h->gated ? 2 : 1;
+    m.global2 = h->gate_g;
     e = launch_gemm2(h->tm_xp, m, h->num_sms, s, pdl);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }

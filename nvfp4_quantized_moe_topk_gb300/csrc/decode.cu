@@ -11,8 +11,10 @@
 //   1. warp 0 routes the <= 1024 pairs in shared memory (counts, offsets,
 //      stable permutation), identically in every CTA;
 //   2. the CTA's share of (expert, 16-row tile) items -- up tiles, then down
-//      tiles -- is laid out as one run of 64-wide k-tiles per phase and cut
-//      evenly over the warps (a warp's range may start or end inside a tile);
+//      tiles; two consecutive row tiles per item once an expert holds two or
+//      more tokens -- is laid out as one run of 64-wide k-tiles per phase and
+//      cut evenly over the warps (a warp's range may start or end inside an
+//      item);
 //   3. each warp streams its range through a private ring of slots; a slot
 //      holds a chunk of up to 4 weight k-tiles and the matching activation row
 //      segments of up to 8 tokens, all copied by 1-D bulk copies completing on
@@ -23,6 +25,9 @@
 //      fragments of warp-level bf16 MMAs with fp32 accumulation; the last warp
 //      holding part of a tile sums the parts in warp order and writes it:
 //      relu^2 + bf16 rounding fused into the up store, fp32 rows for down;
+//      a gated expert's up item is its gate tile and its up tile of the same
+//      16 rows (the TensorFold gate-up kernel's "both rows"), and the store
+//      is bf16(silu(gate) * up);
 //   5. one grid barrier (a single arrival per CTA) separates up from down; the
 //      weight chunks of the first down tiles are already in flight across it,
 //      their activation rows (the relu^2 rows) are requested right after it;
@@ -176,7 +181,7 @@ struct DecodeCtx {
   int32_t split;            // 1: each phase's k-tiles are cut evenly over the warps (one pass of <= 8 tokens)
   int32_t u_lo, n_up, d_lo, n_dn;  // this CTA's items per phase
   int32_t KTu, KTd, NTu, NTd;
-  int32_t pairs;            // 1: a work item is two consecutive row tiles, 0: one
+  int32_t pu, pd;           // per phase, 1: a work item is two consecutive row tiles, 0: one
   int32_t NPu, NPd;         // work items per expert
   uint32_t wbytes;          // weight bytes of a ring slot (the activation rows follow)
   int32_t Wu, Wd;           // warps that take part in each phase (split mode)
@@ -188,7 +193,7 @@ struct DecodeCtx {
     const int32_t lo = c.ph ? d_lo : u_lo, NP = c.ph ? NPd : NPu;
     const int32_t flat = lo + c.i;
     const int32_t ei = flat / NP;
-    c.rt = (flat - ei * NP) << pairs;  // first row tile of the item
+    c.rt = (flat - ei * NP) << (c.ph ? pd : pu);  // first row tile of the item
     c.e = s_act[ei];
     c.cnt = s_counts[c.e];
     c.off = s_off[c.e];
@@ -254,7 +259,9 @@ struct DecodeCtx {
     return base + ((size_t)((size_t)c.e * NT + c.rt) * KT + c.kt) * kTileBytes;
   }
   __device__ __forceinline__ int32_t kts(const Cur& c) const { return min(kDecCK, c.kt_end - c.kt); }
-  __device__ __forceinline__ bool two(const Cur& c) const { return pairs && c.rt + 1 < (c.ph ? NTd : NTu); }
+  __device__ __forceinline__ bool two(const Cur& c) const {
+    return (c.ph ? pd : pu) && c.rt + 1 < (c.ph ? NTd : NTu);
+  }
   // Lane 0 only: declare the chunk's bytes (the k-tiles of both row tiles and
   // the activation rows, the latter possibly issued later) and bulk-copy the
   // weight tiles: row tile rt into the slot's first half, rt + 1 (the next
@@ -507,6 +514,21 @@ __device__ __forceinline__ void decode_epilogue(const DecodeCtx& cx, const Cur& 
   const int g = lane >> 2, t = lane & 3;
   const float alpha = (up ? a.up_g : a.dn_g)[cur.e] * 256.0f;
   const int32_t nt = min(kDecPassTok, cur.cnt - cur.tok0);
+  if (up && a.gated) {
+    // the pair is (gate tile, up tile) of the same 16 intermediate rows
+    const float ag = a.gate_g[cur.e] * 256.0f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int32_t col = 2 * t + (q & 1);
+      const int32_t row = (cur.rt >> 1) * 16 + g + 8 * (q >> 1);
+      if (col < nt) {
+        const size_t pr = (size_t)(cur.off + cur.tok0 + col);
+        const float gv = v[q] * ag;
+        a.Ap[pr * a.I + row] = f2bf_rn(gv / (1.0f + expf(-gv)) * (v[4 + q] * alpha));
+      }
+    }
+    return;
+  }
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
     const int32_t col = 2 * t + (q & 1);
@@ -623,9 +645,10 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) decode_kernel(const __gr
   const uint32_t nt_cap = (uint32_t)max(1, min(kDecPassTok, cmax));
   // two row tiles per work item once an expert has several tokens (their
   // activation fragments are then loaded once for both); single tiles keep
-  // the chunks small where the layer is all latency
-  const int32_t pairs = cmax >= 2;
-  const uint32_t wbytes = pairs ? kDecSlotBytes : kDecCK * kTileBytes;
+  // the chunks small where the layer is all latency.  A gated up projection
+  // always takes its gate and up tiles together.
+  const int32_t pd = cmax >= 2, pu = pd || a.gated;
+  const uint32_t wbytes = pu ? kDecSlotBytes : kDecCK * kTileBytes;
   const uint32_t slot_bytes = wbytes + nt_cap * kDecActRow;
   const uint32_t ring_bytes = L.total - L.ring;
   const int32_t Weff = max(1, min(W, (int32_t)(ring_bytes / (2u * slot_bytes))));
@@ -634,9 +657,9 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) decode_kernel(const __gr
   DecodeCtx cx(a);
   cx.s_tok = s_tok; cx.s_counts = s_counts; cx.s_off = s_off; cx.s_act = s_act;
   cx.warp = warp; cx.W = Weff;
-  cx.KTu = a.H / 64; cx.KTd = a.I / 64; cx.NTu = a.I / 16; cx.NTd = a.H / 16;
-  cx.pairs = pairs; cx.wbytes = wbytes;
-  cx.NPu = (cx.NTu + pairs) >> pairs; cx.NPd = (cx.NTd + pairs) >> pairs;
+  cx.KTu = a.H / 64; cx.KTd = a.I / 64; cx.NTu = (a.gated ? 2 * a.I : a.I) / 16; cx.NTd = a.H / 16;
+  cx.pu = pu; cx.pd = pd; cx.wbytes = wbytes;
+  cx.NPu = (cx.NTu + pu) >> pu; cx.NPd = (cx.NTd + pd) >> pd;
   {
     const int64_t G = gridDim.x, b = blockIdx.x;
     const int64_t U = (int64_t)n_act * cx.NPu, D = (int64_t)n_act * cx.NPd;

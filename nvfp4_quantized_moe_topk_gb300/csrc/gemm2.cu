@@ -29,7 +29,11 @@
 //               tcgen05.st into the A stage of its TMEM lane; a warp signals a
 //               stage ready only after unpacking its next k-block, so the
 //               store's latency hides behind that work
-//   warps 20-23 epilogue: tcgen05.ld, alpha, fp32 rows or bf16(relu^2) rows
+//   warps 20-23 epilogue: tcgen05.ld, alpha, fp32 rows or bf16(relu^2) rows;
+//               for a gated expert the weight rows come in groups of 16 gate
+//               rows then the 16 up rows of the same features, so TMEM lanes
+//               l and l + 16 of a warp meet in one shuffle per two token
+//               columns and store bf16(silu(gate) * up)
 //
 // TMEM columns: accumulators [0,192) and [192,384), four 32-column A stages
 // from 384.  Tiles are (expert, 192 packed rows, 128 features), features
@@ -533,6 +537,37 @@ __global__ void __launch_bounds__(g2::kThreads, 1)
       const bool live = f < a.N;
       const float alpha = a.global[ti.g] * 256.0f;  // the unpacked weights carry 2^-8
       const int32_t ncols = (ti.rows + 15) & ~15;
+      if (a.epilogue == 2) {
+        // lanes 0-15 hold the gate rows of features n0/2 + 16q + lane, lanes
+        // 16-31 the up rows.  Per pair of token columns (i, i+1) one shuffle
+        // hands the low half the up value of column i and the high half the
+        // gate value of column i+1, so every lane finishes one output.
+        const bool lo = lane < 16;
+        const float ah = lo ? a.global2[ti.g] * 256.0f : alpha;
+        const int32_t NO = a.N / 2;
+        const int32_t fo = ti.n0 / 2 + 16 * q + (lane & 15);
+        for (int32_t c0 = 0; c0 < ncols; c0 += 16) {
+          uint32_t r[16];
+          tmem_ld16(tmem_base + ((uint32_t)(32 * q) << 16) + acc * g2::kAccCols + c0, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; i += 2) {
+            const float h0 = ah * __uint_as_float(r[i]), h1 = ah * __uint_as_float(r[i + 1]);
+            const float got = __shfl_xor_sync(0xffffffffu, lo ? h1 : h0, 16);
+            const float gv = lo ? h0 : got, uv = lo ? got : h1;
+            const int32_t tok = c0 + i + (lo ? 0 : 1);
+            // silu(g) = g / (1 + e^-g), fast exponential and divide: the
+            // result is rounded to bf16, far coarser than their error
+            const float av = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
+            if (tok < ti.rows && live)
+              reinterpret_cast<uint16_t*>(a.out)[(size_t)(ti.row0 + tok) * NO + fo] = f2bf_rn(av);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tmem_empty[acc]);
+        continue;
+      }
       for (int32_t c0 = 0; c0 < ncols; c0 += 16) {
         uint32_t r[16];
         tmem_ld16(tmem_base + ((uint32_t)(32 * q) << 16) + acc * g2::kAccCols + c0, r);

@@ -14,7 +14,8 @@
 // bf16 activations with fp32 fused multiply-adds, and reduced across the warp
 // with shuffles in a fixed butterfly order, so results are run-to-run
 // identical.  relu^2 and the bf16 rounding of the up projection are fused
-// into the store.
+// into the store.  For a gated expert the warp streams the gate row and the
+// up row of the same feature together and stores bf16(silu(gate) * up).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -81,6 +82,51 @@ __device__ __forceinline__ void load_row(RowChunks& r, const uint8_t* codes_row,
   }
 }
 
+// One row's partial dot products against the pass's tokens (this lane's chunks).
+__device__ __forceinline__ void row_dots(const RowChunks& rc, const uint32_t* lut_lane, const uint32_t* scale_lut,
+                                         const uint16_t* const (&xrow)[kGemvTok], int nt, int nchunks, int lane,
+                                         float (&acc)[kGemvTok]) {
+#pragma unroll
+  for (int i = 0; i < kGemvMaxChunks; ++i) {
+    const int ch = lane + 32 * i;
+    if (ch < nchunks) {
+      const uint32_t s0 = scale_lut[rc.s[i] & 0xFFu], s1 = scale_lut[(rc.s[i] >> 8) & 0xFFu];
+      const uint32_t words[4] = {rc.c[i].x, rc.c[i].y, rc.c[i].z, rc.c[i].w};
+      uint32_t w[16];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const uint32_t byte = (words[q] >> (8 * b)) & 0xFFu;
+          w[4 * q + b] = hmul2_bf16(lut_lane[byte * 32], q < 2 ? s0 : s1);
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < kGemvTok; ++t) {
+        if (t < nt) {
+          const uint4* xp = reinterpret_cast<const uint4*>(xrow[t] + 32 * ch);
+          uint4 xv[4];
+#pragma unroll
+          for (int v = 0; v < 4; ++v) xv[v] = __ldg(xp + v);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            fma2_bf16(acc[t], w[4 * v + 0], xv[v].x);
+            fma2_bf16(acc[t], w[4 * v + 1], xv[v].y);
+            fma2_bf16(acc[t], w[4 * v + 2], xv[v].z);
+            fma2_bf16(acc[t], w[4 * v + 3], xv[v].w);
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < kGemvTok; ++t) {
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], d);
+  }
+}
+
+template <bool GATED>
 __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(GemvArgs a) {
   __shared__ uint32_t lut[256 * 32];       // [code byte][lane]: bf16x2 (low nibble, high nibble)
   __shared__ uint32_t scale_lut[256];      // e4m3 byte -> bf16x2 (s, s)
@@ -135,12 +181,13 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(GemvArgs a) {
   const long long nwarps = (long long)gridDim.x * kGemvWarps;
   const uint32_t* lut_lane = lut + lane;
 
-  RowChunks cur, nxt;
+  RowChunks cur, nxt, gcur, gnxt;
   long long u = gwarp;
   if (u < total) {
     const int e = act[u / N], n = (int)(u % N);
     const size_t wr = (size_t)e * N + n;
     load_row(cur, a.codes + wr * code_row, a.scales + wr * scale_row, nchunks, lane);
+    if (GATED) load_row(gcur, a.gate_codes + wr * code_row, a.gate_scales + wr * scale_row, nchunks, lane);
   }
   for (; u < total; u += nwarps) {
     const int e = act[u / N], n = (int)(u % N);
@@ -149,6 +196,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(GemvArgs a) {
       const int e2 = act[un / N], n2 = (int)(un % N);
       const size_t wr = (size_t)e2 * N + n2;
       load_row(nxt, a.codes + wr * code_row, a.scales + wr * scale_row, nchunks, lane);
+      if (GATED) load_row(gnxt, a.gate_codes + wr * code_row, a.gate_scales + wr * scale_row, nchunks, lane);
     }
     const int cnt = a.counts[e], off = a.offsets[e];
     const float g = a.global[e];
@@ -161,54 +209,21 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(GemvArgs a) {
         const long long src = a.token_indexed ? (long long)(a.perm_pair[r] / a.k) : (long long)r;
         xrow[t] = a.in + (size_t)src * K;
       }
-      float acc[kGemvTok];
+      float acc[kGemvTok], gacc[kGemvTok];
 #pragma unroll
-      for (int t = 0; t < kGemvTok; ++t) acc[t] = 0.f;
-#pragma unroll
-      for (int i = 0; i < kGemvMaxChunks; ++i) {
-        const int ch = lane + 32 * i;
-        if (ch < nchunks) {
-          const uint32_t s0 = scale_lut[cur.s[i] & 0xFFu], s1 = scale_lut[(cur.s[i] >> 8) & 0xFFu];
-          const uint32_t words[4] = {cur.c[i].x, cur.c[i].y, cur.c[i].z, cur.c[i].w};
-          uint32_t w[16];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {
-              const uint32_t byte = (words[q] >> (8 * b)) & 0xFFu;
-              w[4 * q + b] = hmul2_bf16(lut_lane[byte * 32], q < 2 ? s0 : s1);
-            }
-          }
-#pragma unroll
-          for (int t = 0; t < kGemvTok; ++t) {
-            if (t < nt) {
-              const uint4* xp = reinterpret_cast<const uint4*>(xrow[t] + 32 * ch);
-              uint4 xv[4];
-#pragma unroll
-              for (int v = 0; v < 4; ++v) xv[v] = __ldg(xp + v);
-#pragma unroll
-              for (int v = 0; v < 4; ++v) {
-                fma2_bf16(acc[t], w[4 * v + 0], xv[v].x);
-                fma2_bf16(acc[t], w[4 * v + 1], xv[v].y);
-                fma2_bf16(acc[t], w[4 * v + 2], xv[v].z);
-                fma2_bf16(acc[t], w[4 * v + 3], xv[v].w);
-              }
-            }
-          }
-        }
-      }
-#pragma unroll
-      for (int t = 0; t < kGemvTok; ++t) {
-#pragma unroll
-        for (int d = 16; d >= 1; d >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], d);
-      }
+      for (int t = 0; t < kGemvTok; ++t) acc[t] = gacc[t] = 0.f;
+      row_dots(cur, lut_lane, scale_lut, xrow, nt, nchunks, lane, acc);
+      if (GATED) row_dots(gcur, lut_lane, scale_lut, xrow, nt, nchunks, lane, gacc);
       // lane t stores token t of this pass
 #pragma unroll
       for (int t = 0; t < kGemvTok; ++t) {
         if (lane == t && t < nt) {
           const size_t o = (size_t)(off + t0 + t) * N + n;
           const float h = g * acc[t];
-          if (a.relu2_bf16_out) {
+          if (GATED) {
+            const float gv = a.gate_global[e] * gacc[t];
+            reinterpret_cast<uint16_t*>(a.out)[o] = f2bf_rn(gv / (1.0f + expf(-gv)) * h);
+          } else if (a.relu2_bf16_out) {
             const float r = fmaxf(h, 0.f);
             reinterpret_cast<uint16_t*>(a.out)[o] = f2bf_rn(r * r);
           } else {
@@ -218,6 +233,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(GemvArgs a) {
       }
     }
     cur = nxt;
+    if (GATED) gcur = gnxt;
   }
 }
 
@@ -226,7 +242,8 @@ cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t s, bool pdl) {
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int grid = sms * 4;
-  return launch_ex(gemv_kernel, dim3(grid), dim3(kGemvThreads), 0, s, pdl, a);
+  if (a.gate_codes) return launch_ex(gemv_kernel<true>, dim3(grid), dim3(kGemvThreads), 0, s, pdl, a);
+  return launch_ex(gemv_kernel<false>, dim3(grid), dim3(kGemvThreads), 0, s, pdl, a);
 }
 
 }  // namespace moe

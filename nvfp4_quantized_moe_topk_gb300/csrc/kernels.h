@@ -42,6 +42,10 @@ struct GemvArgs {
   int32_t max_rows;        // experts with 0 < count <= max_rows take this path (<= 0: every expert)
   int32_t token_indexed;   // 1: input row of packed row r is in[perm_pair[r] / k]
   int32_t relu2_bf16_out;  // 1: out = bf16(max(g*acc,0)^2); 0: out = fp32 g*acc
+  // non-null: gated up projection, out = bf16(silu(gg*gate_acc) * g*acc)
+  const uint8_t* gate_codes;   // [E][N][K/2]
+  const uint8_t* gate_scales;  // [E][N][K/16]
+  const float* gate_global;    // [E]
 };
 cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t s, bool pdl);
 
@@ -77,8 +81,10 @@ struct Gemm2Args {
   const int32_t* offsets;  // [G+1]
   int32_t G, N, K;
   int32_t min_rows;        // groups with count > min_rows take this path
-  void* out;               // [rows][N]: fp32 (epilogue 0) or bf16 relu^2 (epilogue 1)
+  void* out;               // [rows][N]: fp32 (epilogue 0) or bf16 relu^2 (epilogue 1);
+                           // [rows][N/2] bf16 silu(gate) * up (epilogue 2)
   int32_t epilogue;
+  const float* global2;    // [G] gate alpha (epilogue 2: rows in groups of 16 gate then 16 up)
   int32_t* err;
 };
 // tmX: bf16 activations [rows][K], box 64 x 192, 128-byte swizzle.
@@ -135,10 +141,12 @@ inline DecLayout dec_layout(int32_t E, int32_t R, uint32_t budget) {
 }
 
 struct DecodeArgs {
-  const uint8_t* up_tiles;    // [E][I/16][H/64][576]
+  const uint8_t* up_tiles;    // [E][I/16][H/64][576]; gated: [E][2I/16][H/64][576], gate and up tiles alternating
   const uint8_t* dn_tiles;    // [E][H/16][I/64][576]
   const float* up_g;
   const float* dn_g;
+  const float* gate_g;        // gated only
+  int32_t gated;              // 1: a = bf16(silu(gate) * up), else bf16(relu(up)^2)
   const uint16_t* x;          // [n][H] bf16
   const int32_t* ids;         // [n][k]
   const float* tw;            // [n][k]

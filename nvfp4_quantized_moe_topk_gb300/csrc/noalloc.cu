@@ -6,7 +6,7 @@
 // a fixed memory budget decided at load time, and callers that must not
 // trigger the implicit device synchronisation cudaMalloc may cause.  For them
 // this entry point takes the weights and activations as given and keeps every
-// intermediate (routing arrays, relu^2 rows, down rows, error flag) in one
+// intermediate (routing arrays, relu^2 or silu*up rows, down rows, error flag) in one
 // file-scope __device__ array of fixed size, which every GPU that loads the
 // library holds until the process exits.
 //
@@ -49,6 +49,10 @@ extern "C" moe_status moe_nvfp4_forward_noalloc(const moe_nvfp4_config* config, 
   if (!x || !topk_ids || !topk_weights || !dst || !w->up_codes || !w->up_scales || !w->down_codes ||
       !w->down_scales || !w->up_global || !w->down_global)
     return MOE_ERR_INVALID_ARG;
+  if (config->activation != MOE_ACT_RELU2 && config->activation != MOE_ACT_SWIGLU) return MOE_ERR_INVALID_ARG;
+  const bool gated = config->activation == MOE_ACT_SWIGLU;
+  if (gated && (!w->gate_codes || !w->gate_scales || !w->gate_global)) return MOE_ERR_INVALID_ARG;
+  if (gated && reinterpret_cast<uintptr_t>(w->gate_codes) % 16) return MOE_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(dst) |
        reinterpret_cast<uintptr_t>(w->up_codes) | reinterpret_cast<uintptr_t>(w->down_codes)) % 16)
     return MOE_ERR_INVALID_ARG;
@@ -114,7 +118,15 @@ extern "C" moe_status moe_nvfp4_forward_noalloc(const moe_nvfp4_config* config, 
   g.K = H;
   g.token_indexed = 1;
   g.relu2_bf16_out = 1;
+  if (gated) {
+    g.gate_codes = w->gate_codes;
+    g.gate_scales = w->gate_scales;
+    g.gate_global = w->gate_global;
+  }
   if (moe::launch_gemv(g, s, true) != cudaSuccess) return MOE_ERR_CUDA;
+  g.gate_codes = nullptr;
+  g.gate_scales = nullptr;
+  g.gate_global = nullptr;
   g.codes = w->down_codes;
   g.scales = w->down_scales;
   g.global = w->down_global;

@@ -19,13 +19,18 @@ def bf16_from_dev(t) -> np.ndarray:
 
 def make_layer(wl, dev, max_tokens=None, gemv_max_rows=0, stream=None, single_max_tokens=0):
     """single_max_tokens=-1 forces the multi-kernel path (routing, gather,
-    streaming kernel for small experts, grouped GEMMs, combine)."""
+    streaming kernel for small experts, grouped GEMMs, combine).  A workload
+    with gate weights makes a gated layer."""
     from nvfp4_quantized_moe_topk_gb300 import api
 
+    gate = {}
+    if getattr(wl, "gate_codes", None) is not None:
+        gate = dict(gate_codes=to_dev(wl.gate_codes, dev), gate_scales=to_dev(wl.gate_scales, dev),
+                    gate_global=to_dev(wl.gate_global, dev))
     return api.MoeLayer(wl.H, wl.I, wl.E, wl.k, wl.n if max_tokens is None else max_tokens,
                         to_dev(wl.up_codes, dev), to_dev(wl.up_scales, dev), to_dev(wl.down_codes, dev),
                         to_dev(wl.down_scales, dev), to_dev(wl.up_global, dev), to_dev(wl.down_global, dev),
-                        gemv_max_rows=gemv_max_rows, single_max_tokens=single_max_tokens, stream=stream)
+                        gemv_max_rows=gemv_max_rows, single_max_tokens=single_max_tokens, stream=stream, **gate)
 
 
 def run_forward(layer, wl, dev, stream=None):

@@ -76,6 +76,17 @@ def test_create_validates_shapes_first(lib):
         assert h.value is None
     c = api.Config(256, 128, 8, 2, 32, 0)
     assert lib.moe_nvfp4_create(ctypes.byref(c), None, None, ctypes.byref(h)) == 1
+    # activation: not one of the MOE_ACT_ values / gated without gate weights
+    c = api.Config(256, 128, 8, 2, 32, 0, 0, 7)
+    assert lib.moe_nvfp4_create(ctypes.byref(c), ctypes.byref(w), None, ctypes.byref(h)) == 1
+    c = api.Config(256, 128, 8, 2, 32, 0, 0, api.ACT_SWIGLU)
+    assert lib.moe_nvfp4_create(ctypes.byref(c), ctypes.byref(w), None, ctypes.byref(h)) == 1
+    assert h.value is None
+    wg = api.Weights(16, 16, 16, 16, 16, 16, 16, None, 16)
+    assert lib.moe_nvfp4_create(ctypes.byref(c), ctypes.byref(wg), None, ctypes.byref(h)) == 1
+    vp = ctypes.c_void_p
+    assert lib.moe_nvfp4_forward_noalloc(ctypes.byref(c), ctypes.byref(w), vp(16), vp(16), vp(16), vp(16), 4,
+                                         None) == 1
 
 
 def test_library_is_built_for_sm103a_only():
