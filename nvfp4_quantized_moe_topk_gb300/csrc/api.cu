@@ -75,6 +75,7 @@ struct moe_nvfp4 {
   int32_t *col_done = nullptr, *grid_bar = nullptr;
   // workspace (max_tokens)
   int32_t *counts = nullptr, *offsets = nullptr, *perm_pair = nullptr, *inv = nullptr, *err = nullptr;
+  int32_t* blk_hist = nullptr;  // per-slice expert histograms of the routing kernels
   uint16_t *Xp = nullptr, *Ap = nullptr;
   float* Yp = nullptr;
   // staging for forward_host
@@ -100,7 +101,7 @@ void free_handle(moe_nvfp4* h) {
                   h->counts,   h->offsets,   h->perm_pair, h->inv,      h->err,       h->Xp,
                   h->Ap,       h->Yp,        h->x_stage,   h->dst_stage, h->ids_stage, h->w_stage,
                   h->up_tiles, h->dn_tiles,  h->col_done,  h->grid_bar,  h->up_blocks, h->dn_blocks,
-                  h->gate_codes, h->gate_scales, h->gate_g};
+                  h->gate_codes, h->gate_scales, h->gate_g, h->blk_hist};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   for (auto& s : h->slots) {
@@ -223,6 +224,7 @@ moe_status moe_nvfp4_create(const moe_nvfp4_config* config, const moe_nvfp4_weig
   TRY(cudaMalloc(&h->perm_pair, Rr * sizeof(int32_t)));
   TRY(cudaMalloc(&h->inv, Rr * sizeof(int32_t)));
   TRY(cudaMalloc(&h->err, sizeof(int32_t)));
+  TRY(cudaMalloc(&h->blk_hist, (routing_scratch_ints((int64_t)Rr, (int)E) + 1) * sizeof(int32_t)));
   TRY(cudaMalloc(&h->Xp, Rr * H * 2));
   TRY(cudaMalloc(&h->Ap, Rr * I * 2));
   TRY(cudaMalloc(&h->Yp, Rr * H * 4));
@@ -339,7 +341,7 @@ static moe_status forward_impl(moe_nvfp4* h, const uint16_t* x, const int32_t* i
   }
   {
     TimedLaunch tl(h, s, kKRouting);
-    e = launch_routing(ids, R, E, h->counts, h->offsets, h->perm_pair, h->inv, h->err, s);
+    e = launch_routing(ids, R, E, h->counts, h->offsets, h->perm_pair, h->inv, h->err, s, h->blk_hist);
   }
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   if (gemm) {

@@ -8,9 +8,13 @@
 namespace moe {
 
 // ---------------------------------------------------------------- routing
+// Pairs per routing slice (one CTA each); batches of more than one slice need
+// routing_scratch_ints(R, E) ints of device scratch for the slice histograms.
+constexpr int kRoutingSlice = 4096;
 size_t routing_smem_bytes(int E);
+size_t routing_scratch_ints(int64_t R, int E);
 cudaError_t launch_routing(const int32_t* ids, int32_t R, int32_t E, int32_t* counts, int32_t* offsets,
-                           int32_t* perm_pair, int32_t* inv, int32_t* err, cudaStream_t s);
+                           int32_t* perm_pair, int32_t* inv, int32_t* err, cudaStream_t s, int32_t* blk_hist);
 
 // ------------------------------------------------------------------ router
 // ids/w [n][k] from fp32 logits [n][E] (+ bias [E] or nullptr); counts [E]

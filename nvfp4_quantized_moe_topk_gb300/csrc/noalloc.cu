@@ -57,7 +57,7 @@ extern "C" moe_status moe_nvfp4_forward_noalloc(const moe_nvfp4_config* config, 
        reinterpret_cast<uintptr_t>(w->up_codes) | reinterpret_cast<uintptr_t>(w->down_codes)) % 16)
     return MOE_ERR_INVALID_ARG;
 
-  // Carve the fixed array: routing arrays, error flag, relu^2 rows, down rows.
+  // Carve the fixed array: routing arrays, error flag, slice histograms, relu^2 rows, down rows.
   const size_t R = (size_t)n_tokens * k;
   size_t off = 0;
   const size_t o_counts = off;
@@ -70,6 +70,8 @@ extern "C" moe_status moe_nvfp4_forward_noalloc(const moe_nvfp4_config* config, 
   off = round_up(off + 4 * R, 256);
   const size_t o_err = off;
   off = round_up(off + 4, 256);
+  const size_t o_blk = off;
+  off = round_up(off + 4 * (moe::routing_scratch_ints((int64_t)R, E) + 1), 256);
   const size_t o_ap = off;
   off = round_up(off + 2 * R * (size_t)I, 256);
   const size_t o_yp = off;
@@ -93,6 +95,7 @@ extern "C" moe_status moe_nvfp4_forward_noalloc(const moe_nvfp4_config* config, 
   int32_t* perm = reinterpret_cast<int32_t*>(base + o_perm);
   int32_t* inv = reinterpret_cast<int32_t*>(base + o_inv);
   int32_t* err = reinterpret_cast<int32_t*>(base + o_err);
+  int32_t* blk_hist = reinterpret_cast<int32_t*>(base + o_blk);
   uint16_t* Ap = reinterpret_cast<uint16_t*>(base + o_ap);
   float* Yp = reinterpret_cast<float*>(base + o_yp);
 
@@ -100,7 +103,7 @@ extern "C" moe_status moe_nvfp4_forward_noalloc(const moe_nvfp4_config* config, 
   // The error flag is the only piece of the array that must start at zero
   // (the kernels overwrite every other word they read).
   if (cudaMemsetAsync(err, 0, sizeof(int32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
-  if (moe::launch_routing(topk_ids, (int32_t)R, E, counts, offsets, perm, inv, err, s) != cudaSuccess)
+  if (moe::launch_routing(topk_ids, (int32_t)R, E, counts, offsets, perm, inv, err, s, blk_hist) != cudaSuccess)
     return MOE_ERR_CUDA;
   moe::GemvArgs g{};
   g.counts = counts;

@@ -89,6 +89,30 @@ def test_routing_flags_and_drops_bad_ids(dev):
     layer.close()
 
 
+@pytest.mark.parametrize("n,k,E,seed", [(1500, 6, 40, 5), (700, 8, 8, 6)])
+def test_routing_slices_drop_and_flag_bad_ids(dev, n, k, E, seed):
+    """Several 4096-pair slices (histogram kernel + per-slice scatter), with
+    out-of-range ids scattered over all of them: bit-exact and flagged."""
+    rng = np.random.default_rng(seed)
+    ids = rng.integers(0, E, size=(n, k)).astype(np.int32)
+    bad = rng.random((n, k)) < 0.01
+    ids[bad] = rng.choice(np.array([-1, -5, E, E + 3], np.int32), size=int(bad.sum()))
+    wl = W.Workload("r", n, 64, 64, E, k, None, ids, None, np.zeros((E, 64, 32), np.uint8),
+                    np.full((E, 64, 4), 0x38, np.uint8), np.zeros((E, 64, 32), np.uint8),
+                    np.full((E, 64, 4), 0x38, np.uint8), np.ones(E, np.float32), np.ones(E, np.float32), None)
+    layer = make_layer(wl, dev, gemv_max_rows=1 << 30)
+    c, o, p, i = _gpu_routing(layer, wl, dev, ids)
+    rc, ro, rp, ri, dropped = oracle.routing(ids, E)
+    assert dropped == int(bad.sum()) > 0
+    kept = n * k - dropped
+    assert np.array_equal(c, rc) and np.array_equal(o, ro)
+    assert np.array_equal(p[:kept], rp) and np.array_equal(i, ri)
+    from nvfp4_quantized_moe_topk_gb300 import api
+
+    assert layer.device_error() & api.DEVFLAG_BAD_ROUTING
+    layer.close()
+
+
 def test_weighted_row_sum_hand_fixtures(dev):
     import torch
 

@@ -61,3 +61,24 @@ def test_noalloc_rejects_oversized_batches():
     with pytest.raises(api.MoeError) as ei:
         api.forward_noalloc(wl.H, wl.I, wl.E, wl.k, *weights, x, ids, tw, dst)
     assert ei.value.status == 3
+
+
+def test_noalloc_several_routing_slices():
+    """5600 pairs at small shapes: the routing's slice histograms live in the
+    fixed array too; checked against the oracle."""
+    import torch
+
+    import oracle
+    from nvfp4_quantized_moe_topk_gb300 import api
+
+    api.load(build_if_missing=True)
+    dev = torch.device("cuda:0")
+    wl = W.small_custom(700, 64, 64, 8, 8, seed=80)
+    weights = [to_dev(a, dev) for a in (wl.up_codes, wl.up_scales, wl.down_codes, wl.down_scales,
+                                         wl.up_global, wl.down_global)]
+    got = to_dev(wl.dst, dev)
+    api.forward_noalloc(wl.H, wl.I, wl.E, wl.k, *weights, to_dev(wl.x, dev), to_dev(wl.topk_ids, dev),
+                        to_dev(wl.topk_weights, dev), got)
+    torch.cuda.synchronize()
+    ok, err, rms = layer_tolerance_check(bf16_from_dev(got), oracle.moe_forward(wl).dst)
+    assert ok, (err, rms)
