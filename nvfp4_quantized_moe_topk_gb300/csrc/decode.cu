@@ -142,13 +142,15 @@ __device__ __forceinline__ uint4 ld_cg_v4(const void* p) {
   asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
   return v;
 }
-__device__ __forceinline__ int32_t ld_acquire_gpu(const int32_t* p) {
-  int32_t v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
+__device__ __forceinline__ uint64_t atom_add_acq_rel_gpu_u64(uint64_t* p, uint64_t v) {
+  uint64_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
+  return old;
 }
-__device__ __forceinline__ void red_release_gpu_add(int32_t* p, int32_t v) {
-  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+__device__ __forceinline__ uint64_t ld_acquire_gpu_u64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
 }
 __device__ __forceinline__ void all_warps_sync(int nthreads) {
   asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
@@ -442,17 +444,23 @@ __device__ __forceinline__ void decode_select(const DecodeArgs& a, int lane, int
   }
 }
 
-// One arrival per CTA, then poll until the arrival count reaches `want`
-// (gridDim.x for the first barrier of a launch, 2 * gridDim.x for the second).
-__device__ __forceinline__ void decode_grid_barrier(const DecodeArgs& a, int tid, int nthreads, int32_t want) {
+// Grid barrier on one 64-bit arrival counter that only grows: every launch
+// runs gridDim.x CTAs and each barrier takes one arrival per CTA, so a
+// barrier ends when the count reaches the next multiple of gridDim.x after
+// the arrival.  The arrival is acquire-release (this CTA's stores, ordered
+// before by the CTA barrier, travel with it) and the polls are acquire loads.
+// Nothing needs resetting when the launch ends, so the kernel finishes
+// without a final round of atomics.
+__device__ __forceinline__ void decode_grid_barrier(const DecodeArgs& a, int tid, int nthreads) {
   all_warps_sync(nthreads);
   if (tid == 0) {
-    // release: this CTA's stores (ordered before by the CTA barrier) become
-    // visible with the arrival; acquire: other CTAs' stores are visible after
-    red_release_gpu_add(&a.grid_bar[0], 1);
-    if (ld_acquire_gpu(&a.grid_bar[0]) < want) {
+    uint64_t* count = reinterpret_cast<uint64_t*>(a.grid_bar);
+    const uint64_t G = gridDim.x;
+    const uint64_t old = atom_add_acq_rel_gpu_u64(count, 1);
+    const uint64_t target = (old / G + 1) * G;
+    if (old + 1 != target) {
       const uint64_t t0 = globaltimer_ns();
-      while (ld_acquire_gpu(&a.grid_bar[0]) < want) {
+      while (ld_acquire_gpu_u64(count) < target) {
         if (globaltimer_ns() - t0 > kWaitLimitNs) {
           atomicOr(a.err, kFlagTimeout);
           break;
@@ -716,7 +724,7 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) decode_kernel(const __gr
     const Cur cur = wdesc[slot];
     if (cur.ph == 1 && !crossed) {
       // every up tile of every CTA is stored before any down tile reads Ap
-      decode_grid_barrier(a, tid, nthreads, (int32_t)gridDim.x);
+      decode_grid_barrier(a, tid, nthreads);
       crossed = true;
       for (int32_t q = acts_issued; q < issued; ++q) {
         const int32_t s = q % P;
@@ -766,25 +774,17 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) decode_kernel(const __gr
       decode_epilogue(cx, cur, v, lane, partial, pcount, s_inv, n_act);
     }
   }
-  if (!crossed) decode_grid_barrier(a, tid, nthreads, (int32_t)gridDim.x);
+  if (!crossed) decode_grid_barrier(a, tid, nthreads);
   if (dead) {
     // let this warp's copies still in flight land before the CTA exits
     for (int32_t q = consumed; q < issued; ++q) mbar_wait_sleep(&wbar[q % P], (uint32_t)((q / P) & 1), a.err);
   }
   if (!a.ext && a.n > kDecLateCombine) {
     // every down row of every CTA is stored: combine, one element per thread
-    decode_grid_barrier(a, tid, nthreads, 2 * (int32_t)gridDim.x);
+    decode_grid_barrier(a, tid, nthreads);
     const int64_t total = (int64_t)a.n * a.H, stride = (int64_t)gridDim.x * nthreads;
     for (int64_t idx = (int64_t)blockIdx.x * nthreads + tid; idx < total; idx += stride)
       combine_one(a, s_inv, (int32_t)(idx / a.H), (int32_t)(idx % a.H));
-  }
-  all_warps_sync(nthreads);
-  if (tid == 0) {
-    __threadfence();
-    if (atomicAdd(&a.grid_bar[1], 1) == (int32_t)gridDim.x - 1) {
-      a.grid_bar[0] = 0;
-      a.grid_bar[1] = 0;
-    }
   }
 }
 

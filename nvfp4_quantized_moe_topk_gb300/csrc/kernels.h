@@ -162,7 +162,7 @@ struct DecodeArgs {
   int32_t* g_perm;
   int32_t* g_inv;
   int32_t* col_done;          // [H/16] combine counters, zero between launches
-  int32_t* grid_bar;          // {arrivals, exits}, zero between launches
+  int32_t* grid_bar;          // 8-byte aligned: one 64-bit arrival count (multiple of the grid between launches)
   int32_t* err;
   int32_t n, H, I, E, k;
   // ext = 1: routing comes from g_counts / g_offsets / g_perm (written by the
