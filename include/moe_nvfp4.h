@@ -165,6 +165,22 @@ MOE_API moe_status moe_nvfp4_forward_host(moe_nvfp4_t handle, const uint16_t *x_
                                   const float *topk_weights_host, uint16_t *dst_host, int32_t n_tokens,
                                   moe_stream_t stream);
 
+/* The shared expert: the same expert FFN applied to every token with weight 1,
+ * WRITING its output to dst (the pre-filled dst that moe_nvfp4_forward adds
+ * the routed experts onto; pull request #91, "What changes", WeightedRowSum
+ * "onto the shared expert's" output):
+ *     dst[t] = bf16_rne(y(x[t]))      y as at the top of the file, expert 0
+ * The handle must have been created with n_experts = 1 and top_k = 1 (its
+ * weights are the shared expert's); it runs the same kernels as
+ * moe_nvfp4_forward, with every token routed to expert 0 at weight 1 onto a
+ * zeroed dst.  x device bf16 [n][H], dst device bf16 [n][H] (written).
+ * Enqueues a memset of dst and the forward on `stream`; capturable in the same
+ * CUDA graph as the routed layer's forward that follows it.
+ * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED (handle not 1 expert,
+ * top-1), MOE_ERR_CAPACITY, MOE_ERR_CUDA. */
+MOE_API moe_status moe_nvfp4_shared_expert_forward(moe_nvfp4_t handle, const uint16_t *x, uint16_t *dst,
+                                                   int32_t n_tokens, moe_stream_t stream);
+
 /* Reads and clears the handle's device error flags (MOE_DEVFLAG_* bits).
  * Synchronizes the device. */
 MOE_API moe_status moe_nvfp4_get_device_error(moe_nvfp4_t handle, int32_t *flags);

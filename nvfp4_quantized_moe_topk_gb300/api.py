@@ -24,7 +24,8 @@ DEVFLAG_TIMEOUT = 0x2
 ENTRY_POINTS = ("moe_nvfp4_status_string", "moe_nvfp4_create", "moe_nvfp4_destroy", "moe_nvfp4_forward",
                 "moe_nvfp4_forward_host", "moe_nvfp4_get_device_error", "moe_nvfp4_debug_routing",
                 "moe_nvfp4_debug_intermediates", "moe_nvfp4_set_timing", "moe_nvfp4_kernel_times",
-                "nvfp4_matmul", "weighted_row_sum", "moe_nvfp4_forward_noalloc", "moe_router_topk")
+                "nvfp4_matmul", "weighted_row_sum", "moe_nvfp4_forward_noalloc", "moe_router_topk",
+                "moe_nvfp4_shared_expert_forward")
 
 _lock = threading.Lock()
 _lib = None
@@ -75,6 +76,7 @@ def load(build_if_missing: bool = False):
         L.moe_nvfp4_destroy.argtypes = [vp]
         L.moe_nvfp4_forward.argtypes = [vp, vp, vp, vp, vp, i32, vp]
         L.moe_nvfp4_forward_host.argtypes = [vp, vp, vp, vp, vp, i32, vp]
+        L.moe_nvfp4_shared_expert_forward.argtypes = [vp, vp, vp, i32, vp]
         L.moe_nvfp4_get_device_error.argtypes = [vp, ctypes.POINTER(i32)]
         L.moe_nvfp4_debug_routing.argtypes = [vp, vp, vp, vp, vp, vp]
         L.moe_nvfp4_debug_intermediates.argtypes = [vp, vp, vp, vp]
@@ -151,6 +153,13 @@ class MoeLayer:
         n = x.shape[0] if n_tokens is None else n_tokens
         _check(load().moe_nvfp4_forward(self._h, _ptr(x), _ptr(topk_ids), _ptr(topk_weights), _ptr(dst), n,
                                         _stream(stream)), "moe_nvfp4_forward")
+        return dst
+
+    def shared_expert_forward(self, x, dst, n_tokens: int | None = None, stream=None):
+        """dst = bf16(expert 0's FFN of x) for a 1-expert top-1 layer (the shared expert)."""
+        n = x.shape[0] if n_tokens is None else n_tokens
+        _check(load().moe_nvfp4_shared_expert_forward(self._h, _ptr(x), _ptr(dst), n, _stream(stream)),
+               "moe_nvfp4_shared_expert_forward")
         return dst
 
     def forward_host(self, x, topk_ids, topk_weights, dst, n_tokens: int | None = None, stream=None):

@@ -76,6 +76,9 @@ struct moe_nvfp4 {
   // workspace (max_tokens)
   int32_t *counts = nullptr, *offsets = nullptr, *perm_pair = nullptr, *inv = nullptr, *err = nullptr;
   int32_t* blk_hist = nullptr;  // per-slice expert histograms of the routing kernels
+  // one-expert top-1 handles (shared expert): every token to expert 0 at weight 1
+  int32_t* dense_ids = nullptr;
+  float* dense_w = nullptr;
   uint16_t *Xp = nullptr, *Ap = nullptr;
   float* Yp = nullptr;
   // staging for forward_host
@@ -101,7 +104,7 @@ void free_handle(moe_nvfp4* h) {
                   h->counts,   h->offsets,   h->perm_pair, h->inv,      h->err,       h->Xp,
                   h->Ap,       h->Yp,        h->x_stage,   h->dst_stage, h->ids_stage, h->w_stage,
                   h->up_tiles, h->dn_tiles,  h->col_done,  h->grid_bar,  h->up_blocks, h->dn_blocks,
-                  h->gate_codes, h->gate_scales, h->gate_g, h->blk_hist};
+                  h->gate_codes, h->gate_scales, h->gate_g, h->blk_hist, h->dense_ids, h->dense_w};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   for (auto& s : h->slots) {
@@ -245,6 +248,15 @@ moe_status moe_nvfp4_create(const moe_nvfp4_config* config, const moe_nvfp4_weig
   TRY(cudaMemcpyAsync(h->up_g, w->up_global, E * sizeof(float), cudaMemcpyDeviceToDevice, s));
   TRY(cudaMemcpyAsync(h->dn_g, w->down_global, E * sizeof(float), cudaMemcpyDeviceToDevice, s));
   TRY(cudaMemsetAsync(h->err, 0, sizeof(int32_t), s));
+  if (E == 1 && c.top_k == 1) {
+    const size_t nt = c.max_tokens > 0 ? (size_t)c.max_tokens : 1;
+    TRY(cudaMalloc(&h->dense_ids, nt * sizeof(int32_t)));
+    TRY(cudaMalloc(&h->dense_w, nt * sizeof(float)));
+    TRY(cudaMemsetAsync(h->dense_ids, 0, nt * sizeof(int32_t), s));
+    std::vector<float> ones(nt, 1.0f);
+    TRY(cudaMemcpyAsync(h->dense_w, ones.data(), nt * sizeof(float), cudaMemcpyHostToDevice, s));
+    TRY(cudaStreamSynchronize(s));  // `ones` leaves scope
+  }
   TRY(cudaMemsetAsync(h->counts, 0, E * sizeof(int32_t), s));
   TRY(cudaMemsetAsync(h->offsets, 0, (E + 1) * sizeof(int32_t), s));
   TRY(cudaMemsetAsync(h->Ap, 0, Rr * I * 2, s));
@@ -450,6 +462,18 @@ moe_status moe_nvfp4_forward(moe_nvfp4_t h, const uint16_t* x, const int32_t* id
   if (!x || !ids || !tw || !dst) return MOE_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(dst, 16) || !aligned(ids, 4) || !aligned(tw, 4)) return MOE_ERR_INVALID_ARG;
   return forward_impl(h, x, ids, tw, dst, n, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_nvfp4_shared_expert_forward(moe_nvfp4_t h, const uint16_t* x, uint16_t* dst, int32_t n,
+                                           moe_stream_t stream) {
+  if (!h || n < 0) return MOE_ERR_INVALID_ARG;
+  if (h->cfg.n_experts != 1 || h->cfg.top_k != 1 || !h->dense_ids) return MOE_ERR_UNSUPPORTED;
+  if (n > h->cfg.max_tokens) return MOE_ERR_CAPACITY;
+  if (n == 0) return MOE_OK;
+  if (!x || !dst || !aligned(x, 16) || !aligned(dst, 16)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(dst, 0, (size_t)n * h->cfg.hidden * 2, s) != cudaSuccess) return MOE_ERR_CUDA;
+  return forward_impl(h, x, h->dense_ids, h->dense_w, dst, n, s);
 }
 
 moe_status moe_nvfp4_forward_host(moe_nvfp4_t h, const uint16_t* x, const int32_t* ids, const float* tw,

@@ -4,6 +4,8 @@ Every case edits one spot of ``oracle/moe_oracle.c``, compiles the edited copy
 under ``oracle/_build/``, routes the oracle through it, and expects the named
 pin test to fail.  A pin set that lets any of these through is too weak.
 """
+import os
+
 import pytest
 
 import oracle
@@ -116,10 +118,13 @@ def test_planted_mistake_is_caught(name, old, new, catchers):
     src = oracle.source_text()
     assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
     path = oracle.build_variant(src.replace(old, new), name)
-    with oracle.use_library(path):
-        for catch in catchers:
-            with pytest.raises((AssertionError, ValueError)):
-                catch()
+    try:
+        with oracle.use_library(path):
+            for catch in catchers:
+                with pytest.raises((AssertionError, ValueError)):
+                    catch()
+    finally:
+        os.remove(path)  # the loaded copy stays mapped; only the file goes
     # the unmutated oracle still passes the same pins
     for catch in catchers:
         catch()
