@@ -142,6 +142,11 @@ __device__ __forceinline__ uint4 ld_cg_v4(const void* p) {
   asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
   return v;
 }
+__device__ __forceinline__ int32_t atom_add_acq_rel_gpu(int32_t* p, int32_t v) {
+  int32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
 __device__ __forceinline__ uint64_t atom_add_acq_rel_gpu_u64(uint64_t* p, uint64_t v) {
   uint64_t old;
   asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
@@ -553,19 +558,22 @@ __device__ __forceinline__ void decode_epilogue(const DecodeCtx& cx, const Cur& 
     }
   }
   if (up || a.ext || a.n > kDecLateCombine || cur.tok0 + kDecPassTok < cur.cnt) return;
-  // down tiles complete: count each against its 16 columns
-  __threadfence();
+  // down tiles complete: count each against its 16 columns.  The warp
+  // barrier orders every lane's row stores before lane 0's acquire-release
+  // count, which publishes them (cumulatively) to the last counter of the
+  // block; its acquire, and the warp barrier after it, make every tile's
+  // rows visible to the lanes that combine them.
   __syncwarp();
   for (int h = 0; h < (pair ? 2 : 1); ++h) {
     const int32_t rt = cur.rt + h;
     int32_t last = 0;
     if (lane == 0) {
-      last = atomicAdd(&a.col_done[rt], 1) == n_act - 1;
+      last = atom_add_acq_rel_gpu(&a.col_done[rt], 1) == n_act - 1;
       if (last) a.col_done[rt] = 0;
     }
     last = __shfl_sync(0xffffffffu, last, 0);
     if (!last) continue;
-    __threadfence();
+    __syncwarp();
     const int32_t c = rt * 16 + (lane & 15);
     for (int32_t tk = lane >> 4; tk < a.n; tk += 2) {
       uint16_t* d = a.dst + (size_t)tk * a.H + c;
