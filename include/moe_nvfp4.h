@@ -159,7 +159,10 @@ MOE_API moe_status moe_nvfp4_forward(moe_nvfp4_t handle, const uint16_t *x, cons
 
 /* Same layer on HOST buffers (pinned memory gives full copy speed): copies
  * x, ids, weights and dst to handle-owned device staging buffers, runs the
- * forward, copies dst back and synchronizes `stream` before returning.
+ * forward, copies dst back and synchronizes `stream` before returning.  When
+ * the four inputs total at most 64 KB (decode-sized batches) they are first
+ * packed on the host into one handle-owned pinned buffer, so one copy moves
+ * them in and one moves dst out.
  * Same arguments and errors as moe_nvfp4_forward. */
 MOE_API moe_status moe_nvfp4_forward_host(moe_nvfp4_t handle, const uint16_t *x_host, const int32_t *topk_ids_host,
                                   const float *topk_weights_host, uint16_t *dst_host, int32_t n_tokens,

@@ -54,6 +54,9 @@ struct TimingSlot {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+constexpr size_t kSmallStage = 64 * 1024;  // bytes; below this a host call packs its inputs
+size_t round16(size_t v) { return (v + 15) & ~size_t(15); }
+
 }  // namespace
 
 struct moe_nvfp4 {
@@ -85,6 +88,9 @@ struct moe_nvfp4 {
   uint16_t *x_stage = nullptr, *dst_stage = nullptr;
   int32_t* ids_stage = nullptr;
   float* w_stage = nullptr;
+  // small host calls: the four inputs packed in one pinned host buffer and
+  // moved by one copy each way (nullptr if the pinned allocation failed)
+  uint8_t *small_dev = nullptr, *small_host = nullptr;
   // tensor maps
   CUtensorMap tm_xp{}, tm_ap{};  // 192-row activation tiles of the grouped GEMM
   int32_t last_n = 0;
@@ -107,6 +113,8 @@ void free_handle(moe_nvfp4* h) {
                   h->gate_codes, h->gate_scales, h->gate_g, h->blk_hist, h->dense_ids, h->dense_w};
   for (void* p : ptrs)
     if (p) cudaFree(p);
+  if (h->small_dev) cudaFree(h->small_dev);
+  if (h->small_host) cudaFreeHost(h->small_host);
   for (auto& s : h->slots) {
     if (s.beg) cudaEventDestroy(s.beg);
     if (s.end) cudaEventDestroy(s.end);
@@ -235,6 +243,11 @@ moe_status moe_nvfp4_create(const moe_nvfp4_config* config, const moe_nvfp4_weig
   TRY(cudaMalloc(&h->dst_stage, (size_t)(c.max_tokens > 0 ? c.max_tokens : 1) * H * 2));
   TRY(cudaMalloc(&h->ids_stage, Rr * sizeof(int32_t)));
   TRY(cudaMalloc(&h->w_stage, Rr * sizeof(float)));
+  TRY(cudaMalloc(&h->small_dev, kSmallStage));
+  if (cudaMallocHost(&h->small_host, kSmallStage) != cudaSuccess) {
+    h->small_host = nullptr;  // host calls then copy each array on its own
+    cudaGetLastError();
+  }
   TRY(cudaMalloc(&h->up_tiles, (mat_codes + mat_scales) * (gated ? 2 : 1)));
   TRY(cudaMalloc(&h->dn_tiles, mat_codes + mat_scales));
   TRY(cudaMalloc(&h->up_blocks, gemm_blocks_bytes((int32_t)E, (int32_t)up_rows, (int32_t)H)));
@@ -484,6 +497,26 @@ moe_status moe_nvfp4_forward_host(moe_nvfp4_t h, const uint16_t* x, const int32_
   if (!x || !ids || !tw || !dst) return MOE_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const size_t H = h->cfg.hidden, R = (size_t)n * h->cfg.top_k;
+  const size_t bx = (size_t)n * H * 2, bi = R * 4;
+  const size_t oi = round16(bx), ow = oi + round16(bi), od = ow + round16(bi), total = od + bx;
+  if (h->small_host && total <= kSmallStage) {
+    // one pinned copy each way instead of four in and one out
+    std::memcpy(h->small_host, x, bx);
+    std::memcpy(h->small_host + oi, ids, bi);
+    std::memcpy(h->small_host + ow, tw, bi);
+    std::memcpy(h->small_host + od, dst, bx);
+    if (cudaMemcpyAsync(h->small_dev, h->small_host, total, cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    uint16_t* ddst = reinterpret_cast<uint16_t*>(h->small_dev + od);
+    const moe_status st = forward_impl(h, reinterpret_cast<const uint16_t*>(h->small_dev),
+                                       reinterpret_cast<const int32_t*>(h->small_dev + oi),
+                                       reinterpret_cast<const float*>(h->small_dev + ow), ddst, n, s);
+    if (st != MOE_OK) return st;
+    if (cudaMemcpyAsync(h->small_host + od, ddst, bx, cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+    std::memcpy(dst, h->small_host + od, bx);
+    return MOE_OK;
+  }
   if (cudaMemcpyAsync(h->x_stage, x, (size_t)n * H * 2, cudaMemcpyHostToDevice, s) != cudaSuccess ||
       cudaMemcpyAsync(h->ids_stage, ids, R * 4, cudaMemcpyHostToDevice, s) != cudaSuccess ||
       cudaMemcpyAsync(h->w_stage, tw, R * 4, cudaMemcpyHostToDevice, s) != cudaSuccess ||

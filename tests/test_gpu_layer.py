@@ -169,18 +169,24 @@ def test_zero_and_negative_weights(dev):
     _check_layer(wl, dev)
 
 
-def test_deterministic_and_forward_host_matches(dev):
+@pytest.mark.parametrize("name,pinned", [("decode-32", True), ("decode-1", True), ("tiny", True),
+                                         ("decode-1", False), ("decode-32", False)])
+def test_deterministic_and_forward_host_matches(dev, name, pinned):
+    """Host-buffer calls give the device forward's bits: small ones (inputs
+    <= 64 KB: decode-1, tiny) go through one packed pinned copy each way,
+    larger ones copy each array."""
     import torch
 
-    wl = W.generate("decode-32")
+    wl = W.generate(name)
     layer = make_layer(wl, dev)
     a = run_forward(layer, wl, dev)
     b = run_forward(layer, wl, dev)
     assert np.array_equal(a, b)
-    xh = torch.from_numpy(wl.x.view(np.int16)).pin_memory()
-    ih = torch.from_numpy(wl.topk_ids).pin_memory()
-    wh = torch.from_numpy(wl.topk_weights).pin_memory()
-    dh = torch.from_numpy(wl.dst.view(np.int16).copy()).pin_memory()
+    host = (lambda t: t.pin_memory()) if pinned else (lambda t: t)
+    xh = host(torch.from_numpy(wl.x.view(np.int16)))
+    ih = host(torch.from_numpy(wl.topk_ids))
+    wh = host(torch.from_numpy(wl.topk_weights))
+    dh = host(torch.from_numpy(wl.dst.view(np.int16).copy()))
     layer.forward_host(xh, ih, wh, dh)
     assert np.array_equal(dh.numpy().view(np.uint16), a)
     layer.close()
