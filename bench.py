@@ -475,8 +475,10 @@ def run_ours(args):
     layer.close()
 
     clocks = clk.summary()
-    # single launch; or routing, gather, small experts, 2 GEMMs, combine; or routing, 2 GEMVs, combine
-    launches_per_step = 1 if decode_single_launch(wl.n, wl.k, T) else (6 if wl.n > T else 4)
+    # single launch; or routing (one kernel, or two above 4096 pairs), gather, small experts, 2 GEMMs,
+    # combine; or routing, 2 GEMVs, combine
+    routing_launches = 1 if wl.n * wl.k <= 4096 else 2
+    launches_per_step = 1 if decode_single_launch(wl.n, wl.k, T) else routing_launches + (5 if wl.n > T else 3)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
