@@ -202,6 +202,16 @@ MOE_API moe_status moe_nvfp4_debug_routing(moe_nvfp4_t handle, int32_t *counts, 
 MOE_API moe_status moe_nvfp4_debug_intermediates(moe_nvfp4_t handle, uint16_t *a_rows, float *y_rows,
                                          moe_stream_t stream);
 
+/* Test hook for the failure path: adds `arrivals` to the arrival count of the
+ * streaming kernel's grid barrier (synchronizes the device).  A count that is
+ * no longer a multiple of the grid makes the next single-launch forward's
+ * barrier unable to complete for some CTAs: their bounded wait gives up after
+ * about 2 s, sets MOE_DEVFLAG_TIMEOUT and the launch returns (its output is
+ * then undefined); moe_nvfp4_get_device_error reports the flag and resets the
+ * counters, after which forwards are correct again.  No fault, trap or hang
+ * is involved.  Errors: MOE_ERR_INVALID_ARG, MOE_ERR_CUDA. */
+MOE_API moe_status moe_nvfp4_debug_offset_grid_barrier(moe_nvfp4_t handle, int64_t arrivals);
+
 /* Per-kernel CUDA-event timing of forward (off by default).  While on, each
  * kernel launch of forward is bracketed by an event pair on its stream. */
 MOE_API moe_status moe_nvfp4_set_timing(moe_nvfp4_t handle, int32_t enable);

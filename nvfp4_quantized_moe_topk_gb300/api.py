@@ -25,7 +25,7 @@ ENTRY_POINTS = ("moe_nvfp4_status_string", "moe_nvfp4_create", "moe_nvfp4_destro
                 "moe_nvfp4_forward_host", "moe_nvfp4_get_device_error", "moe_nvfp4_debug_routing",
                 "moe_nvfp4_debug_intermediates", "moe_nvfp4_set_timing", "moe_nvfp4_kernel_times",
                 "nvfp4_matmul", "weighted_row_sum", "moe_nvfp4_forward_noalloc", "moe_router_topk",
-                "moe_nvfp4_shared_expert_forward")
+                "moe_nvfp4_shared_expert_forward", "moe_nvfp4_debug_offset_grid_barrier")
 
 _lock = threading.Lock()
 _lib = None
@@ -77,6 +77,7 @@ def load(build_if_missing: bool = False):
         L.moe_nvfp4_forward.argtypes = [vp, vp, vp, vp, vp, i32, vp]
         L.moe_nvfp4_forward_host.argtypes = [vp, vp, vp, vp, vp, i32, vp]
         L.moe_nvfp4_shared_expert_forward.argtypes = [vp, vp, vp, i32, vp]
+        L.moe_nvfp4_debug_offset_grid_barrier.argtypes = [vp, ctypes.c_int64]
         L.moe_nvfp4_get_device_error.argtypes = [vp, ctypes.POINTER(i32)]
         L.moe_nvfp4_debug_routing.argtypes = [vp, vp, vp, vp, vp, vp]
         L.moe_nvfp4_debug_intermediates.argtypes = [vp, vp, vp, vp]
@@ -154,6 +155,12 @@ class MoeLayer:
         _check(load().moe_nvfp4_forward(self._h, _ptr(x), _ptr(topk_ids), _ptr(topk_weights), _ptr(dst), n,
                                         _stream(stream)), "moe_nvfp4_forward")
         return dst
+
+    def debug_offset_grid_barrier(self, arrivals: int):
+        """Test hook: offset the streaming kernel's barrier count (the next
+        single-launch forward then times out, bounded; see the C header)."""
+        _check(load().moe_nvfp4_debug_offset_grid_barrier(self._h, int(arrivals)),
+               "moe_nvfp4_debug_offset_grid_barrier")
 
     def shared_expert_forward(self, x, dst, n_tokens: int | None = None, stream=None):
         """dst = bf16(expert 0's FFN of x) for a 1-expert top-1 layer (the shared expert)."""

@@ -570,6 +570,16 @@ moe_status moe_nvfp4_debug_intermediates(moe_nvfp4_t h, uint16_t* a_rows, float*
   return cuda_status(e);
 }
 
+moe_status moe_nvfp4_debug_offset_grid_barrier(moe_nvfp4_t h, int64_t arrivals) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+  uint64_t count = 0;
+  if (cudaMemcpy(&count, h->grid_bar, sizeof(count), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  count += (uint64_t)arrivals;
+  if (cudaMemcpy(h->grid_bar, &count, sizeof(count), cudaMemcpyHostToDevice) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
 moe_status moe_nvfp4_set_timing(moe_nvfp4_t h, int32_t enable) {
   if (!h) return MOE_ERR_INVALID_ARG;
   if (enable && h->slots.empty()) {

@@ -784,7 +784,13 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) decode_kernel(const __gr
   }
   if (!crossed) decode_grid_barrier(a, tid, nthreads);
   if (dead) {
-    // let this warp's copies still in flight land before the CTA exits
+    // let this warp's copies still in flight land before the CTA exits; the
+    // chunks whose activations were never requested get them now (in-bounds
+    // reads of whatever the rows hold) so that their barriers can complete
+    for (int32_t q = acts_issued; q < issued; ++q) {
+      const int32_t s = q % P;
+      cx.issue_acts(wdesc[s], lane, ring + (size_t)s * slot_bytes, &wbar[s]);
+    }
     for (int32_t q = consumed; q < issued; ++q) mbar_wait_sleep(&wbar[q % P], (uint32_t)((q / P) & 1), a.err);
   }
   if (!a.ext && a.n > kDecLateCombine) {

@@ -86,6 +86,7 @@ def test_create_validates_shapes_first(lib):
     assert lib.moe_nvfp4_create(ctypes.byref(c), ctypes.byref(wg), None, ctypes.byref(h)) == 1
     vp = ctypes.c_void_p
     assert lib.moe_nvfp4_shared_expert_forward(None, vp(16), vp(16), 4, None) == 1
+    assert lib.moe_nvfp4_debug_offset_grid_barrier(None, 1) == 1
     assert lib.moe_nvfp4_forward_noalloc(ctypes.byref(c), ctypes.byref(w), vp(16), vp(16), vp(16), vp(16), 4,
                                          None) == 1
 
