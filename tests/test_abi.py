@@ -94,3 +94,19 @@ def test_create_validates_shapes_first(lib):
 def test_library_is_built_for_sm103a_only():
     assert "arch=compute_103a,code=sm_103a" in " ".join(B.ARCH)
     assert os.path.exists(B.LIB)
+
+
+def test_header_is_plain_c(tmp_path):
+    """The boundary header compiles as strict C99 (no C++ or CUDA types in the signatures)."""
+    import shutil
+    import subprocess
+
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not available")
+    src = tmp_path / "use_header.c"
+    src.write_text('#include "moe_nvfp4.h"\nint main(void) { return MOE_OK; }\n')
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", f"-I{inc}", "-fsyntax-only",
+                        str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
