@@ -91,6 +91,10 @@ struct moe_nvfp4 {
   // small host calls: the four inputs packed in one pinned host buffer and
   // moved by one copy each way (nullptr if the pinned allocation failed)
   uint8_t *small_dev = nullptr, *small_host = nullptr;
+  // large host calls: dst's copy in runs on a side stream while the layer
+  // computes; the combine waits for it (nullptr if creation failed)
+  cudaStream_t side = nullptr;
+  cudaEvent_t dst_in = nullptr;
   // tensor maps
   CUtensorMap tm_xp{}, tm_ap{};  // 192-row activation tiles of the grouped GEMM
   int32_t last_n = 0;
@@ -115,6 +119,8 @@ void free_handle(moe_nvfp4* h) {
     if (p) cudaFree(p);
   if (h->small_dev) cudaFree(h->small_dev);
   if (h->small_host) cudaFreeHost(h->small_host);
+  if (h->dst_in) cudaEventDestroy(h->dst_in);
+  if (h->side) cudaStreamDestroy(h->side);
   for (auto& s : h->slots) {
     if (s.beg) cudaEventDestroy(s.beg);
     if (s.end) cudaEventDestroy(s.end);
@@ -248,6 +254,13 @@ moe_status moe_nvfp4_create(const moe_nvfp4_config* config, const moe_nvfp4_weig
     h->small_host = nullptr;  // host calls then copy each array on its own
     cudaGetLastError();
   }
+  if (cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaEventCreateWithFlags(&h->dst_in, cudaEventDisableTiming) != cudaSuccess) {
+    if (h->side) cudaStreamDestroy(h->side);
+    h->side = nullptr;  // host calls then copy dst in order with the rest
+    h->dst_in = nullptr;
+    cudaGetLastError();
+  }
   TRY(cudaMalloc(&h->up_tiles, (mat_codes + mat_scales) * (gated ? 2 : 1)));
   TRY(cudaMalloc(&h->dn_tiles, mat_codes + mat_scales));
   TRY(cudaMalloc(&h->up_blocks, gemm_blocks_bytes((int32_t)E, (int32_t)up_rows, (int32_t)H)));
@@ -322,8 +335,10 @@ moe_status moe_nvfp4_destroy(moe_nvfp4_t h) {
   return MOE_OK;
 }
 
+// dst_ready (may be null): an event that must complete before anything reads
+// dst (the single-launch kernel, or the WeightedRowSum of the multi-kernel path).
 static moe_status forward_impl(moe_nvfp4* h, const uint16_t* x, const int32_t* ids, const float* tw, uint16_t* dst,
-                               int32_t n, cudaStream_t s) {
+                               int32_t n, cudaStream_t s, cudaEvent_t dst_ready = nullptr) {
   const moe_nvfp4_config& c = h->cfg;
   const int32_t k = c.top_k, E = c.n_experts, H = c.hidden, I = c.inter;
   const int32_t R = n * k;
@@ -360,6 +375,7 @@ static moe_status forward_impl(moe_nvfp4* h, const uint16_t* x, const int32_t* i
     // the whole layer in one launch
     d.L = decode_layout(E, R);
     if (d.L.warps >= 4) {
+      if (dst_ready && cudaStreamWaitEvent(s, dst_ready, 0) != cudaSuccess) return MOE_ERR_CUDA;
       TimedLaunch tl(h, s, kKDecode);
       return cuda_status(launch_decode(d, h->num_sms, s));
     }
@@ -459,6 +475,7 @@ static moe_status forward_impl(moe_nvfp4* h, const uint16_t* x, const int32_t* i
     e = launch_gemm2(h->tm_ap, m, h->num_sms, s, pdl);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
+  if (dst_ready && cudaStreamWaitEvent(s, dst_ready, 0) != cudaSuccess) return MOE_ERR_CUDA;
   {
     TimedLaunch tl(h, s, kKCombine);
     e = launch_weighted_row_sum(dst, h->Yp, h->inv, tw, n, k, H, R, s, pdl);
@@ -517,12 +534,26 @@ moe_status moe_nvfp4_forward_host(moe_nvfp4_t h, const uint16_t* x, const int32_
     std::memcpy(dst, h->small_host + od, bx);
     return MOE_OK;
   }
-  if (cudaMemcpyAsync(h->x_stage, x, (size_t)n * H * 2, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-      cudaMemcpyAsync(h->ids_stage, ids, R * 4, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+  // ids, weights and x first (the routing and the gather need them); dst then
+  // goes in on the side stream while the layer computes, and only the step
+  // that reads dst waits for it (starting it after x keeps the two copies
+  // from sharing the link)
+  if (cudaMemcpyAsync(h->ids_stage, ids, R * 4, cudaMemcpyHostToDevice, s) != cudaSuccess ||
       cudaMemcpyAsync(h->w_stage, tw, R * 4, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-      cudaMemcpyAsync(h->dst_stage, dst, (size_t)n * H * 2, cudaMemcpyHostToDevice, s) != cudaSuccess)
+      cudaMemcpyAsync(h->x_stage, x, (size_t)n * H * 2, cudaMemcpyHostToDevice, s) != cudaSuccess)
     return MOE_ERR_CUDA;
-  moe_status st = forward_impl(h, h->x_stage, h->ids_stage, h->w_stage, h->dst_stage, n, s);
+  cudaEvent_t dst_ready = nullptr;
+  const bool one_launch = n <= h->single_max_tokens && (int64_t)R <= kDecMaxPairs;  // reads dst from its start
+  if (h->side && !one_launch) {
+    if (cudaEventRecord(h->dst_in, s) != cudaSuccess || cudaStreamWaitEvent(h->side, h->dst_in, 0) != cudaSuccess ||
+        cudaMemcpyAsync(h->dst_stage, dst, (size_t)n * H * 2, cudaMemcpyHostToDevice, h->side) != cudaSuccess ||
+        cudaEventRecord(h->dst_in, h->side) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    dst_ready = h->dst_in;
+  } else if (cudaMemcpyAsync(h->dst_stage, dst, (size_t)n * H * 2, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+    return MOE_ERR_CUDA;
+  }
+  moe_status st = forward_impl(h, h->x_stage, h->ids_stage, h->w_stage, h->dst_stage, n, s, dst_ready);
   if (st != MOE_OK) return st;
   if (cudaMemcpyAsync(dst, h->dst_stage, (size_t)n * H * 2, cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return MOE_ERR_CUDA;
