@@ -95,6 +95,7 @@ struct moe_nvfp4 {
   // computes; the combine waits for it (nullptr if creation failed)
   cudaStream_t side = nullptr;
   cudaEvent_t dst_in = nullptr;
+  cudaEvent_t part_done[4] = {};  // combine chunks finished (their dst rows go back on the side stream)
   // tensor maps
   CUtensorMap tm_xp{}, tm_ap{};  // 192-row activation tiles of the grouped GEMM
   int32_t last_n = 0;
@@ -120,6 +121,8 @@ void free_handle(moe_nvfp4* h) {
   if (h->small_dev) cudaFree(h->small_dev);
   if (h->small_host) cudaFreeHost(h->small_host);
   if (h->dst_in) cudaEventDestroy(h->dst_in);
+  for (cudaEvent_t ev : h->part_done)
+    if (ev) cudaEventDestroy(ev);
   if (h->side) cudaStreamDestroy(h->side);
   for (auto& s : h->slots) {
     if (s.beg) cudaEventDestroy(s.beg);
@@ -255,7 +258,11 @@ moe_status moe_nvfp4_create(const moe_nvfp4_config* config, const moe_nvfp4_weig
     cudaGetLastError();
   }
   if (cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) != cudaSuccess ||
-      cudaEventCreateWithFlags(&h->dst_in, cudaEventDisableTiming) != cudaSuccess) {
+      cudaEventCreateWithFlags(&h->dst_in, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&h->part_done[0], cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&h->part_done[1], cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&h->part_done[2], cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&h->part_done[3], cudaEventDisableTiming) != cudaSuccess) {
     if (h->side) cudaStreamDestroy(h->side);
     h->side = nullptr;  // host calls then copy dst in order with the rest
     h->dst_in = nullptr;
@@ -337,8 +344,11 @@ moe_status moe_nvfp4_destroy(moe_nvfp4_t h) {
 
 // dst_ready (may be null): an event that must complete before anything reads
 // dst (the single-launch kernel, or the WeightedRowSum of the multi-kernel path).
+// *combine_left (may be null) set: the multi-kernel path stops before its
+// WeightedRowSum and sets *combine_left = true, leaving it to the caller.
 static moe_status forward_impl(moe_nvfp4* h, const uint16_t* x, const int32_t* ids, const float* tw, uint16_t* dst,
-                               int32_t n, cudaStream_t s, cudaEvent_t dst_ready = nullptr) {
+                               int32_t n, cudaStream_t s, cudaEvent_t dst_ready = nullptr,
+                               bool* combine_left = nullptr) {
   const moe_nvfp4_config& c = h->cfg;
   const int32_t k = c.top_k, E = c.n_experts, H = c.hidden, I = c.inter;
   const int32_t R = n * k;
@@ -476,6 +486,10 @@ static moe_status forward_impl(moe_nvfp4* h, const uint16_t* x, const int32_t* i
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
   if (dst_ready && cudaStreamWaitEvent(s, dst_ready, 0) != cudaSuccess) return MOE_ERR_CUDA;
+  if (combine_left) {
+    *combine_left = true;
+    return MOE_OK;
+  }
   {
     TimedLaunch tl(h, s, kKCombine);
     e = launch_weighted_row_sum(dst, h->Yp, h->inv, tw, n, k, H, R, s, pdl);
@@ -553,10 +567,35 @@ moe_status moe_nvfp4_forward_host(moe_nvfp4_t h, const uint16_t* x, const int32_
   } else if (cudaMemcpyAsync(h->dst_stage, dst, (size_t)n * H * 2, cudaMemcpyHostToDevice, s) != cudaSuccess) {
     return MOE_ERR_CUDA;
   }
-  moe_status st = forward_impl(h, h->x_stage, h->ids_stage, h->w_stage, h->dst_stage, n, s, dst_ready);
+  bool combine_left = false;
+  moe_status st = forward_impl(h, h->x_stage, h->ids_stage, h->w_stage, h->dst_stage, n, s, dst_ready,
+                               dst_ready ? &combine_left : nullptr);
   if (st != MOE_OK) return st;
-  if (cudaMemcpyAsync(dst, h->dst_stage, (size_t)n * H * 2, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-    return MOE_ERR_CUDA;
+  if (!combine_left) {
+    if (cudaMemcpyAsync(dst, h->dst_stage, (size_t)n * H * 2, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    return cuda_status(cudaStreamSynchronize(s));
+  }
+  // the WeightedRowSum in four token ranges; each range's rows of dst go back
+  // on the side stream while the next range is combined
+  const int32_t k = h->cfg.top_k;
+  for (int part = 0; part < 4; ++part) {
+    const int32_t t0 = (int32_t)((int64_t)n * part / 4), t1 = (int32_t)((int64_t)n * (part + 1) / 4);
+    if (t1 == t0) continue;
+    {
+      TimedLaunch tl(h, s, kKCombine);
+      if (launch_weighted_row_sum(h->dst_stage + (size_t)t0 * H, h->Yp, h->inv + (size_t)t0 * k,
+                                  h->w_stage + (size_t)t0 * k, t1 - t0, k, (int32_t)H, (int32_t)R, s,
+                                  !h->timing) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    }
+    if (cudaEventRecord(h->part_done[part], s) != cudaSuccess ||
+        cudaStreamWaitEvent(h->side, h->part_done[part], 0) != cudaSuccess ||
+        cudaMemcpyAsync(dst + (size_t)t0 * H, h->dst_stage + (size_t)t0 * H, (size_t)(t1 - t0) * H * 2,
+                        cudaMemcpyDeviceToHost, h->side) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  if (cudaStreamSynchronize(h->side) != cudaSuccess) return MOE_ERR_CUDA;
   return cuda_status(cudaStreamSynchronize(s));
 }
 

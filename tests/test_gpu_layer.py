@@ -192,6 +192,27 @@ def test_deterministic_and_forward_host_matches(dev, name, pinned):
     layer.close()
 
 
+@pytest.mark.parametrize("pinned", [True, False])
+def test_forward_host_multi_kernel_path(dev, pinned):
+    """A batch on the multi-kernel path through host buffers: dst goes in on
+    the side stream and comes back in four combine ranges; same bits as the
+    device forward."""
+    import torch
+
+    wl = W.small_custom(301, 256, 192, 8, 4, seed=21, bias_sigma=1.0)
+    layer = make_layer(wl, dev)
+    a = run_forward(layer, wl, dev)
+    host = (lambda t: t.pin_memory()) if pinned else (lambda t: t)
+    xh = host(torch.from_numpy(wl.x.view(np.int16)))
+    ih = host(torch.from_numpy(wl.topk_ids))
+    wh = host(torch.from_numpy(wl.topk_weights))
+    dh = host(torch.from_numpy(wl.dst.view(np.int16).copy()))
+    layer.forward_host(xh, ih, wh, dh)
+    assert np.array_equal(dh.numpy().view(np.uint16), a)
+    assert layer.device_error() == 0
+    layer.close()
+
+
 def test_n_zero_and_capacity(dev):
     from nvfp4_quantized_moe_topk_gb300 import api
 
