@@ -163,8 +163,9 @@ MOE_API moe_status moe_nvfp4_forward(moe_nvfp4_t handle, const uint16_t *x, cons
  * the four inputs total at most 64 KB (decode-sized batches) they are first
  * packed on the host into one handle-owned pinned buffer, so one copy moves
  * them in and one moves dst out.  Larger calls copy dst in on a handle-owned
- * side stream while the layer computes; only the step that reads dst waits
- * for that copy.
+ * side stream while the layer computes (only the step that reads dst waits
+ * for that copy), and on the multi-kernel path the result comes back in four
+ * token ranges, each copied out while the next is combined.
  * Same arguments and errors as moe_nvfp4_forward. */
 MOE_API moe_status moe_nvfp4_forward_host(moe_nvfp4_t handle, const uint16_t *x_host, const int32_t *topk_ids_host,
                                   const float *topk_weights_host, uint16_t *dst_host, int32_t n_tokens,
