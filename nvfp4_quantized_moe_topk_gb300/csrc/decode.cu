@@ -633,6 +633,26 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) decode_kernel(const __gr
     for (int32_t i = tid; i < R; i += nthreads) s_ids[i] = a.ids[i];
     for (int32_t i = tid; i < E; i += nthreads) s_counts[i] = 0;
   }
+  if (!a.ext && warp == 1 && lane == 0) {
+    // While the routing is worked out, ask L2 for the up weights of the picked
+    // experts (a slice per CTA of their concatenation in pair order), when
+    // they fit well inside L2: the ring's first requests then find them there.
+    const int64_t per = (int64_t)((a.gated ? 2 * a.I : a.I) / 16) * (a.H / 64) * kTileBytes;
+    const int64_t total = (int64_t)R * per;
+    if (total <= kDecEarlyL2Bytes) {
+      int64_t lo = (total * blockIdx.x / gridDim.x) & ~int64_t(15);
+      const int64_t hi = (total * (blockIdx.x + 1) / gridDim.x) & ~int64_t(15);
+      while (lo < hi) {
+        const int32_t j = (int32_t)(lo / per);
+        const int64_t off = lo - (int64_t)j * per;
+        int64_t len = per - off < hi - lo ? per - off : hi - lo;
+        len = len < 65536 ? len : 65536;
+        const int32_t e = __ldg(a.ids + j);
+        if (e >= 0 && e < E && len >= 16) prefetch_l2_bulk(a.up_tiles + (size_t)e * per + off, (uint32_t)(len & ~int64_t(15)));
+        lo += len;
+      }
+    }
+  }
   for (int i = tid; i < 256; i += nthreads) lut[i] = scale_bf16_2p118((uint32_t)i) * 0x10001u;
   for (int i = tid; i < kDecMaxWarps; i += nthreads) pcount[i] = 0;
   if (lane == 0) {

@@ -104,6 +104,7 @@ constexpr int kDecCK = 4;              // k-tiles (of 64) per chunk
 constexpr int kDecSlotBytes = 2 * kDecCK * kTileBytes;  // weights of a chunk: 2 row tiles x kDecCK k-tiles
 constexpr int kDecPassTok = 8;         // tokens per pass over a tile (one n8 MMA block)
 constexpr int kDecL2Ahead = 8;         // chunks past the ring requested into L2 at start
+constexpr long long kDecEarlyL2Bytes = 48ll << 20;  // picked experts' up weights prefetched during routing, at most
 constexpr int kDecLateCombine = 8;     // larger batches combine after a second grid barrier
 constexpr int kDecMaxPairs = 1024;     // batches with at most this many pairs
 constexpr int kDecMaxTokens = 64;      // and tokens run as one launch
