@@ -121,8 +121,14 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
   }
   if (counts) {
     __syncthreads();
-    for (int32_t e = threadIdx.x; e < E; e += blockDim.x)
-      if (s_hist[e]) atomicAdd(&counts[e], s_hist[e]);
+    if (gridDim.x == 1) {
+      // one block routes every token: it writes the whole histogram (no
+      // zeroing launch before it)
+      for (int32_t e = threadIdx.x; e < E; e += blockDim.x) counts[e] = s_hist[e];
+    } else {
+      for (int32_t e = threadIdx.x; e < E; e += blockDim.x)
+        if (s_hist[e]) atomicAdd(&counts[e], s_hist[e]);
+    }
   }
 }
 
@@ -130,7 +136,8 @@ template <int SLOTS>
 cudaError_t launch_router_t(const float* logits, const float* bias, int32_t n, int32_t E, int32_t k, int32_t* ids,
                             float* w, int32_t* counts, cudaStream_t s) {
   // enough warps to hide a token's latency (~5k in flight), up to 8 tokens each
-  // to cut the number of global histogram atomics on large batches
+  // to cut the number of global histogram atomics on large batches (up to
+  // kRouterWarps tokens make one block, which then writes the histogram itself)
   const int32_t tpw = (int32_t)std::max<long long>(1, std::min<long long>(kRouterMaxTokensPerWarp, n / 4864));
   const long long per_block = (long long)kRouterWarps * tpw;
   const long long blocks = ((long long)n + per_block - 1) / per_block;
@@ -143,7 +150,8 @@ cudaError_t launch_router_t(const float* logits, const float* bias, int32_t n, i
 
 cudaError_t launch_router(const float* logits, const float* bias, int32_t n, int32_t E, int32_t k, int32_t* ids,
                           float* w, int32_t* counts, cudaStream_t s) {
-  if (counts) {
+  const bool one_block = n > 0 && n <= kRouterWarps;
+  if (counts && !one_block) {  // blocks add into counts: zero it first
     const cudaError_t e = cudaMemsetAsync(counts, 0, (size_t)E * sizeof(int32_t), s);
     if (e != cudaSuccess) return e;
   }

@@ -89,3 +89,23 @@ def test_router_without_counts_and_empty(dev):
     with pytest.raises(api.MoeError):
         api.router_topk(to_dev(logits, dev), None, torch.zeros((10, 17), dtype=torch.int32, device=dev),
                         torch.zeros((10, 17), dtype=torch.float32, device=dev))
+
+
+@pytest.mark.parametrize("n", [1, 8, 9, 200])
+def test_router_counts_overwrite_stale_values(dev, n):
+    """Up to 8 tokens run as one block that writes the histogram itself, more
+    as several blocks adding into a zeroed one: either way whatever the
+    counts buffer held before is gone."""
+    import torch
+
+    from nvfp4_quantized_moe_topk_gb300 import api
+
+    rng = np.random.Generator(np.random.PCG64(20 + n))
+    logits = rng.standard_normal((n, 96), dtype=np.float32)
+    ids = torch.empty((n, 6), dtype=torch.int32, device=dev)
+    w = torch.empty((n, 6), dtype=torch.float32, device=dev)
+    counts = torch.full((96,), 7, dtype=torch.int32, device=dev)
+    api.router_topk(to_dev(logits, dev), None, ids, w, counts)
+    torch.cuda.synchronize()
+    _, _, rcounts = oracle.router_topk(logits, None, 6)
+    assert np.array_equal(counts.cpu().numpy(), rcounts)
