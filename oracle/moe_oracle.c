@@ -389,6 +389,10 @@ int or_router_topk(const float *logits, const float *bias, int64_t n, int E, int
           best_z = z;
         }
       }
+      if (best < 0) { /* no expert left: k > E, or a broken order rule */
+        free(zp);
+        return OR_ERR_ARG;
+      }
       ids[t * k + j] = best;
       zp[j] = (double)best_z;
       prev_z = best_z;
