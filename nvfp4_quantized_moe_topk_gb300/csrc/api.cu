@@ -97,7 +97,7 @@ struct moe_nvfp4 {
   cudaEvent_t dst_in = nullptr;
   cudaEvent_t part_done[4] = {};  // combine chunks finished (their dst rows go back on the side stream)
   // tensor maps
-  CUtensorMap tm_xp{}, tm_ap{};  // 192-row activation tiles of the grouped GEMM
+  CUtensorMap tm_xp{}, tm_ap{};  // kGemmTileRows-row activation tiles of the grouped GEMM
   int32_t last_n = 0;
   // per-kernel timing
   bool timing = false;
@@ -321,8 +321,8 @@ moe_status moe_nvfp4_create(const moe_nvfp4_config* config, const moe_nvfp4_weig
   }
   TRY(launch_repack_frag(h->dn_codes, h->dn_scales, (int32_t)E, (int32_t)H, (int32_t)I, h->dn_tiles, s));
   TRY(launch_repack_gemm(h->dn_codes, h->dn_scales, (int32_t)E, (int32_t)H, (int32_t)I, h->dn_blocks, s));
-  TRY(make_tmap_act_rows(&h->tm_xp, h->Xp, Rr, H, 192));
-  TRY(make_tmap_act_rows(&h->tm_ap, h->Ap, Rr, I, 192));
+  TRY(make_tmap_act_rows(&h->tm_xp, h->Xp, Rr, H, kGemmTileRows));
+  TRY(make_tmap_act_rows(&h->tm_ap, h->Ap, Rr, I, kGemmTileRows));
   TRY(cudaStreamSynchronize(s));
 #undef TRY
   if (gu) cudaFree(gu);

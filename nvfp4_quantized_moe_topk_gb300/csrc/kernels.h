@@ -75,6 +75,7 @@ cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const Ge
 // ------------------------------------------- grouped GEMM, A operand in TMEM
 // Packed weight blocks [G][ceil(N/128)][K/64] of 4608 bytes (gemm2.cu).
 constexpr uint32_t kGemmBlockBytes = 128 * 32 + 128 * 4;
+constexpr int kGemmTileRows = 224;  // packed rows (tokens) per grouped-GEMM tile
 cudaError_t launch_repack_gemm(const uint8_t* codes, const uint8_t* scales, int32_t G, int32_t N, int32_t K,
                                uint8_t* out, cudaStream_t s);
 size_t gemm_blocks_bytes(int32_t G, int32_t N, int32_t K);
@@ -91,7 +92,7 @@ struct Gemm2Args {
   const float* global2;    // [G] gate alpha (epilogue 2: rows in groups of 16 gate then 16 up)
   int32_t* err;
 };
-// tmX: bf16 activations [rows][K], box 64 x 192, 128-byte swizzle.
+// tmX: bf16 activations [rows][K], box 64 x kGemmTileRows, 128-byte swizzle.
 cudaError_t launch_gemm2(const CUtensorMap& tmX, const Gemm2Args& a, int num_sms, cudaStream_t s, bool pdl);
 cudaError_t make_tmap_act_rows(CUtensorMap* map, const void* base, uint64_t rows, uint64_t K, uint32_t box_rows);
 

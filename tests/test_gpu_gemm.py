@@ -124,10 +124,12 @@ def test_prefill_16384_sampled(dev):
     _layer_vs_oracle(wl, dev, 0, sample=[(0, 4), (9000, 9004), (16380, 16384)])
 
 
-@pytest.mark.parametrize("n,H,I,E,k,T,seed", [(500, 256, 320, 3, 2, 1, 23), (250, 384, 192, 2, 1, 16, 24)])
+@pytest.mark.parametrize("n,H,I,E,k,T,seed", [(500, 256, 320, 3, 2, 1, 23), (250, 384, 192, 2, 1, 16, 24),
+                                               (449, 128, 128, 1, 1, 1, 25), (448, 192, 256, 1, 1, 1, 26)])
 def test_grouped_gemm_token_tiles_and_ragged_features(dev, n, H, I, E, k, T, seed):
-    """Experts of a few hundred rows span several 192-row token tiles (the last
-    one ragged), and I = 320 / H = 384 leave a partial 128-feature block; the
+    """Experts of a few hundred rows span several 224-row token tiles (the last
+    one ragged; 449 rows leave a one-row tile, 448 fill two exactly), and
+    I = 320 / H = 384 leave a partial 128-feature block; the
     relu^2 rows and fp32 down rows must match the oracle as well as dst."""
     import torch
 
