@@ -129,7 +129,8 @@ def profiled_traffic(workload, kernel):
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
-    rec = json.load(open(path)).get(workload)
+    data = json.load(open(path))
+    rec = data.get(f"{workload}:{kernel}") or data.get(workload)
     if not rec or rec.get("kernel") != kernel:
         return None
     csrc = os.path.join(ROOT, "nvfp4_quantized_moe_topk_gb300", "csrc")
