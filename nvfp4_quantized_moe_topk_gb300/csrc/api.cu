@@ -397,7 +397,7 @@ static moe_status forward_impl(moe_nvfp4* h, const uint16_t* x, const int32_t* i
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   if (gemm) {
     TimedLaunch tl(h, s, kKGather);
-    e = launch_gather(x, h->perm_pair, h->offsets + E, R, k, H, h->Xp, s, pdl);
+    e = launch_gather(x, h->inv, n, k, H, R, h->Xp, s, pdl);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
   // Experts with 0 < rows <= threshold: the same streaming kernel, fed by the

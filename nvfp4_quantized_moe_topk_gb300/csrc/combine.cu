@@ -54,21 +54,35 @@ __global__ void __launch_bounds__(kCombineThreads)
   }
 }
 
-// One warp per packed row: Xp[r][:] = x[perm_pair[r] / k][:] (16-byte vectors).
+// One warp per token: x[t] is read once and written to the packed rows of
+// its k pairs (Xp[inv[t*k + j]][:] = x[t][:], pairs with inv = -1 skipped).
+// Token-major, so a token's row is read from memory once rather than once per
+// pair: with x larger than L2 the row-major form read it k times from HBM.
+// Each lane keeps four 16-byte vectors in flight.
 __global__ void __launch_bounds__(kGatherThreads)
-    gather_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm_pair,
-                  const int32_t* __restrict__ kept_rows, int32_t R, int32_t k, int32_t H,
-                  uint16_t* __restrict__ Xp) {
+    gather_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ inv, int32_t n, int32_t k, int32_t H,
+                  int32_t R, uint16_t* __restrict__ Xp) {
   pdl_wait();
-  const int32_t kept = min(R, *kept_rows);
+  constexpr int kU = 4;
   const int lane = threadIdx.x & 31;
   const long long warps = (long long)gridDim.x * (blockDim.x / 32);
   const int vecs = H / 8;
-  for (long long r = (long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); r < kept; r += warps) {
-    const int32_t t = perm_pair[r] / k;
-    const uint4* s = reinterpret_cast<const uint4*>(x + (size_t)t * H);
-    uint4* d = reinterpret_cast<uint4*>(Xp + (size_t)r * H);
-    for (int v = lane; v < vecs; v += 32) d[v] = __ldg(s + v);
+  for (long long t = (long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); t < n; t += warps) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+    for (int v0 = lane; v0 < vecs; v0 += 32 * kU) {
+      uint4 buf[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u)
+        if (v0 + 32 * u < vecs) buf[u] = __ldg(src + v0 + 32 * u);
+      for (int j = 0; j < k; ++j) {
+        const int32_t r = __ldg(inv + t * k + j);
+        if (r < 0 || r >= R) continue;
+        uint4* d = reinterpret_cast<uint4*>(Xp + (size_t)r * H);
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+          if (v0 + 32 * u < vecs) d[v0 + 32 * u] = buf[u];
+      }
+    }
   }
   pdl_launch_dependents();
 }
@@ -92,15 +106,13 @@ cudaError_t launch_weighted_row_sum(uint16_t* dst, const float* src, const int32
                    rows, w, n, k, cols, src_rows);
 }
 
-cudaError_t launch_gather(const uint16_t* x, const int32_t* perm_pair, const int32_t* kept_rows, int32_t R,
-                          int32_t k, int32_t H, uint16_t* Xp, cudaStream_t s, bool pdl) {
-  const long long warps_needed = R;
-  long long blocks = (warps_needed + (kGatherThreads / 32) - 1) / (kGatherThreads / 32);
+cudaError_t launch_gather(const uint16_t* x, const int32_t* inv, int32_t n, int32_t k, int32_t H, int32_t R,
+                          uint16_t* Xp, cudaStream_t s, bool pdl) {
+  long long blocks = ((long long)n + (kGatherThreads / 32) - 1) / (kGatherThreads / 32);
   const long long cap = (long long)sm_count() * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  return launch_ex(gather_kernel, dim3((unsigned)blocks), dim3(kGatherThreads), 0, s, pdl, x, perm_pair, kept_rows,
-                   R, k, H, Xp);
+  return launch_ex(gather_kernel, dim3((unsigned)blocks), dim3(kGatherThreads), 0, s, pdl, x, inv, n, k, H, R, Xp);
 }
 
 }  // namespace moe

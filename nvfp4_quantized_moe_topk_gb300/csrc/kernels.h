@@ -23,9 +23,9 @@ cudaError_t launch_router(const float* logits, const float* bias, int32_t n, int
                           float* w, int32_t* counts, cudaStream_t s);
 
 // ------------------------------------------------------------ gather / combine
-// Xp[r][:] = x[perm_pair[r] / k][:] for r < offsets[E].
-cudaError_t launch_gather(const uint16_t* x, const int32_t* perm_pair, const int32_t* kept_rows, int32_t R,
-                          int32_t k, int32_t H, uint16_t* Xp, cudaStream_t s, bool pdl);
+// Xp[inv[t*k + j]][:] = x[t][:] for every pair with 0 <= inv < R (n tokens).
+cudaError_t launch_gather(const uint16_t* x, const int32_t* inv, int32_t n, int32_t k, int32_t H, int32_t R,
+                          uint16_t* Xp, cudaStream_t s, bool pdl);
 // dst[i][c] = bf16(dst[i][c] + sum_j w[i][j] * src[rows[i][j]][c]), fixed j order.
 cudaError_t launch_weighted_row_sum(uint16_t* dst, const float* src, const int32_t* rows, const float* w,
                                     int32_t n, int32_t k, int32_t cols, int32_t src_rows, cudaStream_t s,
