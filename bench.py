@@ -26,6 +26,7 @@ import json
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -150,7 +151,9 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        # the raw samples: $MOE_CLOCKS_DIR if set, else the system temp directory
+        out_dir = os.environ.get("MOE_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(out_dir, f"moe_clocks_rank{gpu_index}_{os.getpid()}.csv")
 
     def __enter__(self):
         try:
