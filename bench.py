@@ -103,7 +103,7 @@ def algorithmic_work(wl, ids_list, T):
         per["combine"][0] += n * H * 2 * 2 + n * k * H * 4 + n * k * 8
         per["routing"][0] += n * k * 4 * 4
         if gemm_path:
-            per["gather"][0] += n * k * H * 2 * 2
+            per["gather"][0] += n * H * 2 + n * k * H * 2  # x read once per token, one row written per pair
     m = len(ids_list)
     out = {kname: (b / m, f / m) for kname, (b, f) in per.items()}
     if gemm_path:
