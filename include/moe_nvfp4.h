@@ -162,7 +162,9 @@ MOE_API moe_status moe_nvfp4_forward(moe_nvfp4_t handle, const uint16_t *x, cons
  * forward, copies dst back and synchronizes `stream` before returning.  When
  * the four inputs total at most 64 KB (decode-sized batches) they are first
  * packed on the host into one handle-owned pinned buffer, so one copy moves
- * them in and one moves dst out.  Larger calls copy dst in on a handle-owned
+ * them in; when that batch runs as the single launch, the kernel writes the
+ * result straight into the buffer's device-mapped dst copy (no copy out),
+ * otherwise one copy moves dst out.  Larger calls copy dst in on a handle-owned
  * side stream while the layer computes (only the step that reads dst waits
  * for that copy), and on the multi-kernel path the result comes back in four
  * token ranges, each copied out while the next is combined.

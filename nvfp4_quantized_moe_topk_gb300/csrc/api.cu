@@ -91,6 +91,7 @@ struct moe_nvfp4 {
   // small host calls: the four inputs packed in one pinned host buffer and
   // moved by one copy each way (nullptr if the pinned allocation failed)
   uint8_t *small_dev = nullptr, *small_host = nullptr;
+  uint8_t* small_host_dev = nullptr;  // small_host as the device sees it (mapped), or null
   // large host calls: dst's copy in runs on a side stream while the layer
   // computes; the combine waits for it (nullptr if creation failed)
   cudaStream_t side = nullptr;
@@ -256,6 +257,10 @@ moe_status moe_nvfp4_create(const moe_nvfp4_config* config, const moe_nvfp4_weig
   if (cudaMallocHost(&h->small_host, kSmallStage) != cudaSuccess) {
     h->small_host = nullptr;  // host calls then copy each array on its own
     cudaGetLastError();
+  } else if (cudaHostGetDevicePointer(reinterpret_cast<void**>(&h->small_host_dev), h->small_host, 0) !=
+             cudaSuccess) {
+    h->small_host_dev = nullptr;  // not mapped: the result comes back by copy
+    cudaGetLastError();
   }
   if (cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) != cudaSuccess ||
       cudaEventCreateWithFlags(&h->dst_in, cudaEventDisableTiming) != cudaSuccess ||
@@ -346,9 +351,12 @@ moe_status moe_nvfp4_destroy(moe_nvfp4_t h) {
 // dst (the single-launch kernel, or the WeightedRowSum of the multi-kernel path).
 // *combine_left (may be null) set: the multi-kernel path stops before its
 // WeightedRowSum and sets *combine_left = true, leaving it to the caller.
+// dst_out (may be null): where the single-launch kernel writes the result
+// (a device-visible copy of dst, e.g. mapped pinned host memory); *wrote_out
+// tells whether that path ran.  Other paths update dst in place.
 static moe_status forward_impl(moe_nvfp4* h, const uint16_t* x, const int32_t* ids, const float* tw, uint16_t* dst,
                                int32_t n, cudaStream_t s, cudaEvent_t dst_ready = nullptr,
-                               bool* combine_left = nullptr) {
+                               bool* combine_left = nullptr, uint16_t* dst_out = nullptr, bool* wrote_out = nullptr) {
   const moe_nvfp4_config& c = h->cfg;
   const int32_t k = c.top_k, E = c.n_experts, H = c.hidden, I = c.inter;
   const int32_t R = n * k;
@@ -367,6 +375,7 @@ static moe_status forward_impl(moe_nvfp4* h, const uint16_t* x, const int32_t* i
   d.ids = ids;
   d.tw = tw;
   d.dst = dst;
+  d.dst_out = dst;
   d.Ap = h->Ap;
   d.Yp = h->Yp;
   d.g_counts = h->counts;
@@ -386,6 +395,10 @@ static moe_status forward_impl(moe_nvfp4* h, const uint16_t* x, const int32_t* i
     d.L = decode_layout(E, R);
     if (d.L.warps >= 4) {
       if (dst_ready && cudaStreamWaitEvent(s, dst_ready, 0) != cudaSuccess) return MOE_ERR_CUDA;
+      if (dst_out) {
+        d.dst_out = dst_out;
+        if (wrote_out) *wrote_out = true;
+      }
       TimedLaunch tl(h, s, kKDecode);
       return cuda_status(launch_decode(d, h->num_sms, s));
     }
@@ -531,7 +544,9 @@ moe_status moe_nvfp4_forward_host(moe_nvfp4_t h, const uint16_t* x, const int32_
   const size_t bx = (size_t)n * H * 2, bi = R * 4;
   const size_t oi = round16(bx), ow = oi + round16(bi), od = ow + round16(bi), total = od + bx;
   if (h->small_host && total <= kSmallStage) {
-    // one pinned copy each way instead of four in and one out
+    // one pinned copy in instead of four; the single-launch kernel writes the
+    // result straight into the mapped staging copy of dst (whose unwritten
+    // elements already hold the pre-filled values), so nothing is copied out
     std::memcpy(h->small_host, x, bx);
     std::memcpy(h->small_host + oi, ids, bi);
     std::memcpy(h->small_host + ow, tw, bi);
@@ -539,11 +554,15 @@ moe_status moe_nvfp4_forward_host(moe_nvfp4_t h, const uint16_t* x, const int32_
     if (cudaMemcpyAsync(h->small_dev, h->small_host, total, cudaMemcpyHostToDevice, s) != cudaSuccess)
       return MOE_ERR_CUDA;
     uint16_t* ddst = reinterpret_cast<uint16_t*>(h->small_dev + od);
+    uint16_t* hout = h->small_host_dev ? reinterpret_cast<uint16_t*>(h->small_host_dev + od) : nullptr;
+    bool wrote = false;
     const moe_status st = forward_impl(h, reinterpret_cast<const uint16_t*>(h->small_dev),
                                        reinterpret_cast<const int32_t*>(h->small_dev + oi),
-                                       reinterpret_cast<const float*>(h->small_dev + ow), ddst, n, s);
+                                       reinterpret_cast<const float*>(h->small_dev + ow), ddst, n, s, nullptr,
+                                       nullptr, hout, &wrote);
     if (st != MOE_OK) return st;
-    if (cudaMemcpyAsync(h->small_host + od, ddst, bx, cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (!wrote && cudaMemcpyAsync(h->small_host + od, ddst, bx, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
     std::memcpy(dst, h->small_host + od, bx);
     return MOE_OK;

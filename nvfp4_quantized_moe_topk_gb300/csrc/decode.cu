@@ -576,13 +576,13 @@ __device__ __forceinline__ void decode_epilogue(const DecodeCtx& cx, const Cur& 
     __syncwarp();
     const int32_t c = rt * 16 + (lane & 15);
     for (int32_t tk = lane >> 4; tk < a.n; tk += 2) {
-      uint16_t* d = a.dst + (size_t)tk * a.H + c;
-      float acc = __uint_as_float((uint32_t)*d << 16);
+      const size_t o = (size_t)tk * a.H + c;
+      float acc = __uint_as_float((uint32_t)a.dst[o] << 16);
       for (int32_t j = 0; j < a.k; ++j) {
         const int32_t r = s_inv[tk * a.k + j];
         if (r >= 0) acc = __fmaf_rn(a.tw[tk * a.k + j], ld_cg_f32(a.Yp + (size_t)r * a.H + c), acc);
       }
-      *d = f2bf_rn(acc);
+      a.dst_out[o] = f2bf_rn(acc);
     }
   }
 }
@@ -590,8 +590,8 @@ __device__ __forceinline__ void decode_epilogue(const DecodeCtx& cx, const Cur& 
 // dst[t][c] = bf16(dst[t][c] + sum_j w[t][j] * Yp[inv[t][j]][c]) for one
 // element, j in order; the k row loads are issued before the FMA chain.
 __device__ __forceinline__ void combine_one(const DecodeArgs& a, const int32_t* s_inv, int32_t tk, int32_t c) {
-  uint16_t* d = a.dst + (size_t)tk * a.H + c;
-  float acc = __uint_as_float((uint32_t)*d << 16);
+  const size_t o = (size_t)tk * a.H + c;
+  float acc = __uint_as_float((uint32_t)a.dst[o] << 16);
   for (int32_t j0 = 0; j0 < a.k; j0 += 8) {
     int32_t r[8];
     float y[8], w[8];
@@ -606,7 +606,7 @@ __device__ __forceinline__ void combine_one(const DecodeArgs& a, const int32_t* 
     for (int q = 0; q < 8; ++q)
       if (r[q] >= 0) acc = __fmaf_rn(w[q], y[q], acc);
   }
-  *d = f2bf_rn(acc);
+  a.dst_out[o] = f2bf_rn(acc);
 }
 
 __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) decode_kernel(const __grid_constant__ DecodeArgs a) {

@@ -157,6 +157,7 @@ struct DecodeArgs {
   const int32_t* ids;         // [n][k]
   const float* tw;            // [n][k]
   uint16_t* dst;              // [n][H] bf16
+  uint16_t* dst_out;          // [n][H] bf16: where the in-kernel combine writes (dst, or a host-mapped copy of it)
   uint16_t* Ap;               // [R][I] bf16 (workspace)
   float* Yp;                  // [R][H] fp32 (workspace)
   int32_t* g_counts;          // routing results kept for the debug entry point

@@ -256,3 +256,31 @@ def test_concurrent_streams_match_serial(dev, name, single):
         assert np.array_equal(bf16_from_dev(dsts[i]), serial[i]), f"handle {i}"
         assert layers[i].device_error() == 0
         layers[i].close()
+
+
+@pytest.mark.parametrize("case", ["twelve_tokens", "all_ids_invalid", "packed_multi_kernel"])
+def test_forward_host_packed_cases(dev, case):
+    """Small host calls (one packed pinned copy in): the single launch writes
+    the result straight into the mapped staging copy of dst -- with more than 8
+    tokens through the second-barrier combine, and with no valid pair at all
+    (nothing written: the staged pre-filled values are the result); a batch
+    forced onto the multi-kernel path copies dst back instead.  Same bits as
+    the device forward."""
+    import torch
+
+    wl = W.small_custom(12 if case == "twelve_tokens" else 5, 128, 64, 6, 2, seed=23)
+    if case == "all_ids_invalid":
+        wl.topk_ids[:] = -1
+    kw = dict(single_max_tokens=-1) if case == "packed_multi_kernel" else {}
+    layer = make_layer(wl, dev, **kw)
+    a = run_forward(layer, wl, dev)
+    if case == "all_ids_invalid":
+        assert np.array_equal(a, wl.dst)
+    dh = torch.from_numpy(wl.dst.view(np.int16).copy()).pin_memory()
+    layer.forward_host(torch.from_numpy(wl.x.view(np.int16)).pin_memory(),
+                       torch.from_numpy(wl.topk_ids).pin_memory(),
+                       torch.from_numpy(wl.topk_weights).pin_memory(), dh)
+    assert np.array_equal(dh.numpy().view(np.uint16), a)
+    flags = layer.device_error()
+    layer.close()
+    assert flags == 0 or (case == "all_ids_invalid" and flags == 1)  # 1: out-of-range ids reported
