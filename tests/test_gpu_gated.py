@@ -91,10 +91,11 @@ def test_gated_one_expert_many_tokens(dev):
 
 
 @pytest.mark.parametrize("n,H,I,E,k,T,seed", [(300, 256, 192, 8, 4, 8, 65), (129, 1024, 512, 16, 8, 8, 66),
-                                               (600, 128, 64, 4, 2, 0, 67)])
+                                               (600, 128, 64, 4, 2, 0, 67), (449, 128, 128, 1, 1, 1, 68)])
 def test_gated_grouped_gemm_path(dev, n, H, I, E, k, T, seed):
     """Multi-kernel path: experts above T rows on the grouped GEMM (gated
-    epilogue), the others on the streaming kernel in external-routing mode."""
+    epilogue), the others on the streaming kernel in external-routing mode.
+    449 rows on one expert: two full 224-row token tiles and a one-row tile."""
     wl = W.small_custom(n, H, I, E, k, seed, bias_sigma=1.0, gated=True)
     _check(wl, dev, single_max_tokens=-1, gemv_max_rows=T)
 
