@@ -269,6 +269,7 @@ moe_status moe_nvfp4_create(const moe_nvfp4_config* config, const moe_nvfp4_weig
       cudaEventCreateWithFlags(&h->part_done[2], cudaEventDisableTiming) != cudaSuccess ||
       cudaEventCreateWithFlags(&h->part_done[3], cudaEventDisableTiming) != cudaSuccess) {
     if (h->side) cudaStreamDestroy(h->side);
+    if (h->dst_in) cudaEventDestroy(h->dst_in);
     h->side = nullptr;  // host calls then copy dst in order with the rest
     h->dst_in = nullptr;
     cudaGetLastError();
