@@ -825,15 +825,9 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) decode_kernel(const __gr
 DecLayout decode_layout(int32_t E, int32_t R) { return dec_layout(E, R, 227 * 1024 - 1024); }
 
 cudaError_t launch_decode(const DecodeArgs& args, int num_sms, cudaStream_t s) {
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static std::atomic<bool> attr_set[kMaxDevices];
+  cudaError_t e = raise_smem_limit(decode_kernel, 227 * 1024, attr_set);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_set[dev] = true;
-  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)num_sms);
   cfg.blockDim = dim3(args.L.warps * 32);

@@ -446,13 +446,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
 cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a, int num_sms,
                         cudaStream_t s, bool pdl) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e =
-        cudaFuncSetAttribute(nvfp4_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lay::alloc);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<bool> configured[kMaxDevices];
+  cudaError_t e = raise_smem_limit(nvfp4_gemm_kernel, (int)lay::alloc, configured);
+  if (e != cudaSuccess) return e;
   int grid = num_sms;
   if (a.counts == nullptr) {
     const long long tiles = (long long)((a.M + kBM - 1) / kBM) * ((a.N + kBN - 1) / kBN);

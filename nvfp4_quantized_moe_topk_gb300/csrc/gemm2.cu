@@ -604,15 +604,9 @@ __global__ void __launch_bounds__(g2::kThreads, 1)
 }
 
 cudaError_t launch_gemm2(const CUtensorMap& tmX, const Gemm2Args& a, int num_sms, cudaStream_t s, bool pdl) {
-  static bool configured[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static std::atomic<bool> configured[kMaxDevices];
+  cudaError_t e = raise_smem_limit(nvfp4_gemm2_kernel, (int)g2::alloc, configured);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || !configured[dev]) {
-    e = cudaFuncSetAttribute(nvfp4_gemm2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g2::alloc);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) configured[dev] = true;
-  }
   return launch_ex(nvfp4_gemm2_kernel, dim3(num_sms > 0 ? num_sms : 1), dim3(g2::kThreads), g2::alloc, s, pdl, tmX,
                    a);
 }

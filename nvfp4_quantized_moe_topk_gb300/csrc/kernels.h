@@ -5,7 +5,25 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace moe {
+
+// Raises a kernel's dynamic shared-memory limit on the current device, once
+// per device.  The per-device flags are atomics because launches may come from
+// several host threads; two threads setting the attribute at once is harmless.
+constexpr int kMaxDevices = 64;
+template <typename Kernel>
+inline cudaError_t raise_smem_limit(Kernel* kernel, int bytes, std::atomic<bool> (&done)[kMaxDevices]) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool cached = dev >= 0 && dev < kMaxDevices;
+  if (cached && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && cached) done[dev].store(true, std::memory_order_release);
+  return e;
+}
 
 // ---------------------------------------------------------------- routing
 // Pairs per routing slice (one CTA each); batches of more than one slice need

@@ -26,7 +26,7 @@
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB
-constexpr int kMaxDevices = 64;
+using moe::kMaxDevices;
 
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
@@ -52,9 +52,15 @@ extern "C" moe_status moe_nvfp4_forward_noalloc(const moe_nvfp4_config* config, 
   if (config->activation != MOE_ACT_RELU2 && config->activation != MOE_ACT_SWIGLU) return MOE_ERR_INVALID_ARG;
   const bool gated = config->activation == MOE_ACT_SWIGLU;
   if (gated && (!w->gate_codes || !w->gate_scales || !w->gate_global)) return MOE_ERR_INVALID_ARG;
-  if (gated && reinterpret_cast<uintptr_t>(w->gate_codes) % 16) return MOE_ERR_INVALID_ARG;
-  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(dst) |
-       reinterpret_cast<uintptr_t>(w->up_codes) | reinterpret_cast<uintptr_t>(w->down_codes)) % 16)
+  // The kernels read codes, x and dst 16 bytes at a time, scales 2 bytes at a
+  // time and globals, ids and weights as 4-byte words: a pointer off those
+  // boundaries is an argument error, not a misaligned access on the GPU.
+  auto misaligned = [](const void* p, uintptr_t a) { return reinterpret_cast<uintptr_t>(p) % a != 0; };
+  if (misaligned(x, 16) || misaligned(dst, 16) || misaligned(w->up_codes, 16) || misaligned(w->down_codes, 16) ||
+      misaligned(w->up_scales, 2) || misaligned(w->down_scales, 2) || misaligned(w->up_global, 4) ||
+      misaligned(w->down_global, 4) || misaligned(topk_ids, 4) || misaligned(topk_weights, 4))
+    return MOE_ERR_INVALID_ARG;
+  if (gated && (misaligned(w->gate_codes, 16) || misaligned(w->gate_scales, 2) || misaligned(w->gate_global, 4)))
     return MOE_ERR_INVALID_ARG;
 
   // Carve the fixed array: routing arrays, error flag, slice histograms, relu^2 rows, down rows.

@@ -172,15 +172,9 @@ size_t routing_scratch_ints(int64_t R, int E) {
 cudaError_t launch_routing(const int32_t* ids, int32_t R, int32_t E, int32_t* counts, int32_t* offsets,
                            int32_t* perm_pair, int32_t* inv, int32_t* err, cudaStream_t s, int32_t* blk_hist) {
   const size_t smem = routing_smem_bytes(E);
-  static bool configured[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static std::atomic<bool> configured[kMaxDevices];
+  cudaError_t e = raise_smem_limit(routing_kernel, 200 * 1024, configured);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || !configured[dev]) {
-    e = cudaFuncSetAttribute(routing_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) configured[dev] = true;
-  }
   const int64_t G = ((int64_t)R + kRoutingSlice - 1) / kRoutingSlice;
   if (G <= 1 || !blk_hist) {
     if (G > 1) return cudaErrorInvalidValue;  // several slices need the histogram scratch

@@ -27,7 +27,20 @@ same generator, 9. gate codes [E, I, H/2] and 10. gate scale exponents
 [E, I, H/16] as in 4 and 5, so the draws 1-8 are the same with or without a
 gate.
 
-Per-tensor globals are 2^-4 for every expert and matrix.  Top-k takes the k
+Per-tensor globals are 2^-4 for every expert and matrix.
+
+Parity tests also draw the weights over the whole NVFP4 contract rather than
+the configs' narrow recipe (``scales=`` and ``globals=`` of ``small_custom``
+and ``generate``): block scales uniform over every finite E4M3FN byte of both
+signs (``"full"``: zero, subnormals, every mantissa), or over the bytes whose
+exponent field is 0..3 (``"low"``: zero, all subnormals and the smallest
+normals of both signs, so that the subnormal scales carry a large share of the
+result), and one fp32 global per (expert, matrix), all different and none a
+power of two (``"distinct"``).  The distinct globals are drawn after every
+other array (up, then down, then gate), so a workload's codes, routing and
+activations do not depend on the globals chosen.
+
+Top-k takes the k
 largest biased logits of each token (ties to the lower expert index) in
 descending order; the k routing weights are a softmax over those k biased
 logits, computed in fp64 on the host and stored as fp32.  That routing is the
@@ -102,6 +115,55 @@ def e4m3_byte_of_pow2(u: np.ndarray) -> np.ndarray:
     return ((np.asarray(u, dtype=np.int32) + 7) << 3).astype(np.uint8)
 
 
+SCALE_MODES = ("pow2", "full", "low")
+GLOBAL_MODES = ("const", "distinct")
+
+
+def draw_scales(rng, shape, mode: str = "pow2", exp_range=(-4, 2)) -> np.ndarray:
+    """e4m3 block-scale bytes of the given shape.
+
+    ``pow2``: 2^u with u a uniform integer in ``exp_range`` (the configs' recipe);
+    ``full``: uniform over all 254 finite E4M3FN bytes (every byte but the
+    NaNs 0x7F and 0xFF); ``low``: uniform over the 64 bytes whose exponent
+    field is 0..3, both signs."""
+    if mode == "pow2":
+        lo, hi = exp_range
+        return e4m3_byte_of_pow2(rng.integers(lo, hi + 1, size=shape, dtype=np.int32))
+    if mode == "full":
+        i = rng.integers(0, 254, size=shape, dtype=np.int32)
+        return np.where(i < 0x7F, i, i + 1).astype(np.uint8)  # skip 0x7F; 253 -> 0xFE
+    if mode == "low":
+        i = rng.integers(0, 64, size=shape, dtype=np.int32)  # sign | exponent 0..3 | mantissa
+        return (((i >> 5) << 7) | (i & 31)).astype(np.uint8)
+    raise ValueError(f"unknown scale mode {mode!r}")
+
+
+def draw_globals(rng, E: int, base: float) -> np.ndarray:
+    """One fp32 global per expert: base * u, u uniform in [0.5, 2), never a power of two."""
+    g = (np.float64(base) * rng.uniform(0.5, 2.0, size=E)).astype(np.float32)
+    m, _ = np.frexp(g.astype(np.float64))
+    g = np.where(m == 0.5, np.float32(base) * np.float32(1.375), g).astype(np.float32)
+    return g
+
+
+def global_base(scales: str) -> float:
+    """Global magnitude that keeps the layer output well above the N(0,1) dst
+    for the given scale distribution (small scales need larger globals)."""
+    return 4.0 if scales == "low" else GLOBAL_SCALE
+
+
+def _apply_globals(wl, rng, globals_: str, scales: str):
+    if globals_ == "const":
+        return
+    if globals_ != "distinct":
+        raise ValueError(f"unknown globals mode {globals_!r}")
+    base = global_base(scales)
+    wl.up_global = draw_globals(rng, wl.E, base)
+    wl.down_global = draw_globals(rng, wl.E, base)
+    if wl.gate_codes is not None:
+        wl.gate_global = draw_globals(rng, wl.E, base)
+
+
 def route_topk(logits: np.ndarray, k: int) -> tuple[np.ndarray, np.ndarray]:
     """Top-k by descending logit (ties to the lower index), softmax over the k picked.
 
@@ -125,16 +187,18 @@ def make_routing(n: int, E: int, k: int, bias_sigma: float, seed: int) -> tuple[
     return route_topk(logits, k)
 
 
-def _draw_gate(rng, E: int, H: int, I: int, lo: int = -4, hi: int = 2):
+def _draw_gate(rng, E: int, H: int, I: int, lo: int = -4, hi: int = 2, scales: str = "pow2"):
     codes = rng.integers(0, 256, size=(E, I, H // 2), dtype=np.uint8)
-    scales = e4m3_byte_of_pow2(rng.integers(lo, hi + 1, size=(E, I, H // 16), dtype=np.int32))
-    return codes, scales, np.full(E, GLOBAL_SCALE, dtype=np.float32)
+    sc = draw_scales(rng, (E, I, H // 16), scales, (lo, hi))
+    return codes, sc, np.full(E, GLOBAL_SCALE, dtype=np.float32)
 
 
 def generate(name: str, seed: int | None = None, *, n: int | None = None, weights: bool = True,
-             gated: bool = False) -> Workload:
+             gated: bool = False, scales: str = "pow2", globals_: str = "const") -> Workload:
     """Draw the named workload.  ``n`` overrides the token count (same recipe);
-    ``gated`` adds gate weights (drawn last)."""
+    ``gated`` adds gate weights (drawn last); ``scales`` / ``globals_`` widen
+    the weight draws (see the module docstring; the defaults are the configs'
+    recipe)."""
     cfg = dict(CONFIGS[name])
     if n is not None:
         cfg["n"] = int(n)
@@ -149,9 +213,9 @@ def generate(name: str, seed: int | None = None, *, n: int | None = None, weight
     ids, w = route_topk(logits, k)
     if weights:
         up_codes = rng.integers(0, 256, size=(E, I, H // 2), dtype=np.uint8)
-        up_scales = e4m3_byte_of_pow2(rng.integers(-4, 3, size=(E, I, H // 16), dtype=np.int32))
+        up_scales = draw_scales(rng, (E, I, H // 16), scales)
         down_codes = rng.integers(0, 256, size=(E, H, I // 2), dtype=np.uint8)
-        down_scales = e4m3_byte_of_pow2(rng.integers(-4, 3, size=(E, H, I // 16), dtype=np.int32))
+        down_scales = draw_scales(rng, (E, H, I // 16), scales)
     else:
         up_codes = np.zeros((0,), np.uint8)
         up_scales = down_codes = down_scales = up_codes
@@ -160,12 +224,15 @@ def generate(name: str, seed: int | None = None, *, n: int | None = None, weight
     wl = Workload(name, n_, H, I, E, k, x, ids, w, up_codes, up_scales, down_codes, down_scales,
                   g.copy(), g.copy(), dst)
     if gated and weights:
-        wl.gate_codes, wl.gate_scales, wl.gate_global = _draw_gate(rng, E, H, I)
+        wl.gate_codes, wl.gate_scales, wl.gate_global = _draw_gate(rng, E, H, I, scales=scales)
+    if weights:
+        _apply_globals(wl, rng, globals_, scales)
     return wl
 
 
 def small_custom(n: int, H: int, I: int, E: int, k: int, seed: int, *, bias_sigma: float = 0.0,
-                 scale_exp=(-4, 2), gated: bool = False) -> Workload:
+                 scale_exp=(-4, 2), gated: bool = False, scales: str = "pow2",
+                 globals_: str = "const") -> Workload:
     """Same recipe at arbitrary (small) shapes, for parity and edge-case tests."""
     rng = np.random.Generator(np.random.PCG64(seed))
     x = f32_to_bf16_bits(rng.standard_normal((n, H), dtype=np.float32))
@@ -177,15 +244,16 @@ def small_custom(n: int, H: int, I: int, E: int, k: int, seed: int, *, bias_sigm
     ids, w = route_topk(logits, k)
     lo, hi = scale_exp
     up_codes = rng.integers(0, 256, size=(E, I, H // 2), dtype=np.uint8)
-    up_scales = e4m3_byte_of_pow2(rng.integers(lo, hi + 1, size=(E, I, H // 16), dtype=np.int32))
+    up_scales = draw_scales(rng, (E, I, H // 16), scales, (lo, hi))
     down_codes = rng.integers(0, 256, size=(E, H, I // 2), dtype=np.uint8)
-    down_scales = e4m3_byte_of_pow2(rng.integers(lo, hi + 1, size=(E, H, I // 16), dtype=np.int32))
+    down_scales = draw_scales(rng, (E, H, I // 16), scales, (lo, hi))
     dst = f32_to_bf16_bits(rng.standard_normal((n, H), dtype=np.float32))
     g = np.full(E, GLOBAL_SCALE, dtype=np.float32)
     wl = Workload("custom", n, H, I, E, k, x, ids, w, up_codes, up_scales, down_codes, down_scales,
                   g.copy(), g.copy(), dst)
     if gated:
-        wl.gate_codes, wl.gate_scales, wl.gate_global = _draw_gate(rng, E, H, I, lo, hi)
+        wl.gate_codes, wl.gate_scales, wl.gate_global = _draw_gate(rng, E, H, I, lo, hi, scales)
+    _apply_globals(wl, rng, globals_, scales)
     return wl
 
 
@@ -206,7 +274,8 @@ def l2_flush_bytes() -> int:
 
 
 __all__ = [
-    "CONFIGS", "GLOBAL_SCALE", "Workload", "generate", "small_custom", "make_routing", "route_topk",
+    "CONFIGS", "GLOBAL_SCALE", "SCALE_MODES", "GLOBAL_MODES", "Workload", "generate", "small_custom",
+    "make_routing", "route_topk", "draw_scales", "draw_globals", "global_base",
     "f32_to_bf16_bits", "bf16_bits_to_f32", "e4m3_byte_of_pow2", "expected_rows",
     "weight_bytes_per_expert", "l2_flush_bytes",
 ]

@@ -6,9 +6,9 @@ binding) never imports, links or runs anything here, and this package never
 imports the product: the two share only the seeded input generator, which
 holds none of the layer's arithmetic.
 
-``moe_oracle.c`` is the oracle proper (plain C, fp64, OpenMP over tokens);
-this module compiles it with gcc into ``oracle/_build/`` and wraps it with
-ctypes.  ``numpy_ref`` is an independent restatement (dense-masked form,
+``moe_oracle.c`` is the oracle proper (plain C, fp64, OpenMP over independent
+output values); this module compiles it with gcc into ``oracle/_build/`` and
+wraps it with ctypes.  ``numpy_ref`` is an independent restatement (dense-masked form,
 numpy fp64) used to pin the C oracle.
 """
 from __future__ import annotations
@@ -61,9 +61,9 @@ def _bind(L):
     L.or_nvfp4_matmul.restype = _int
     L.or_weighted_row_sum.argtypes = [_ptr, _ptr, _ptr, _ptr, _i64, _int, _i64, _i64]
     L.or_weighted_row_sum.restype = _i64
-    L.or_moe_forward.argtypes = [_i64, _int, _int, _int, _int] + [_ptr] * 13 + [_i64, _i64]
+    L.or_moe_forward.argtypes = [_i64, _int, _int, _int, _int] + [_ptr] * 14 + [_i64, _i64]
     L.or_moe_forward.restype = _int
-    L.or_moe_forward_act.argtypes = [_i64, _int, _int, _int, _int] + [_ptr] * 9 + [_int] + [_ptr] * 7 + [_i64, _i64]
+    L.or_moe_forward_act.argtypes = [_i64, _int, _int, _int, _int] + [_ptr] * 9 + [_int] + [_ptr] * 8 + [_i64, _i64]
     L.or_moe_forward_act.restype = _int
     L.or_router_topk.argtypes = [_ptr, _ptr, _i64, _int, _int, _ptr, _ptr, _ptr]
     L.or_router_topk.restype = _int
@@ -204,10 +204,15 @@ def weighted_row_sum(dst_bf16: np.ndarray, src: np.ndarray, rows: np.ndarray, w:
 
 # ------------------------------------------------------------- whole layer
 class Result:
-    """Oracle output: final dst (bf16 bits), and optional intermediates."""
+    """Oracle output: final dst (bf16 bits), and optional intermediates.
 
-    def __init__(self, dst, a_rows, y_rows, out_f64):
+    a_rows are the bf16 intermediates (relu^2 or silu * up) by packed row,
+    a_f64 the same values before their bf16 rounding, y_rows the fp64 down
+    rows, out_f64 the layer output before its final rounding."""
+
+    def __init__(self, dst, a_rows, y_rows, out_f64, a_f64=None):
         self.dst, self.a_rows, self.y_rows, self.out_f64 = dst, a_rows, y_rows, out_f64
+        self.a_f64 = a_f64
 
 
 def moe_forward(wl, *, intermediates: bool = False, out_f64: bool = False,
@@ -225,6 +230,7 @@ def moe_forward(wl, *, intermediates: bool = False, out_f64: bool = False,
     dst = _c(wl.dst, np.uint16).copy()
     R = n * k
     a_rows = np.zeros((R, I), np.uint16) if intermediates else None
+    a_f64 = np.zeros((R, I), np.float64) if intermediates else None
     y_rows = np.zeros((R, H), np.float64) if intermediates else None
     of = np.zeros((n, H), np.float64) if out_f64 else None
     t0, t1 = tok_range if tok_range is not None else (0, n)
@@ -233,14 +239,14 @@ def moe_forward(wl, *, intermediates: bool = False, out_f64: bool = False,
         gc, gs = _c(wl.gate_codes, np.uint8), _c(wl.gate_scales, np.uint8)
         gg = _c(wl.gate_global, np.float32)
         rc = lib().or_moe_forward_act(n, H, I, E, k, _p(x), _p(ids), _p(w), *[_p(a) for a in arrs], _p(ug),
-                                      _p(dg), 1, _p(gc), _p(gs), _p(gg), _p(dst), _p(a_rows), _p(y_rows), _p(of),
-                                      t0, t1)
+                                      _p(dg), 1, _p(gc), _p(gs), _p(gg), _p(dst), _p(a_rows), _p(a_f64), _p(y_rows),
+                                      _p(of), t0, t1)
     else:
         rc = lib().or_moe_forward(n, H, I, E, k, _p(x), _p(ids), _p(w), *[_p(a) for a in arrs], _p(ug), _p(dg),
-                                  _p(dst), _p(a_rows), _p(y_rows), _p(of), t0, t1)
+                                  _p(dst), _p(a_rows), _p(a_f64), _p(y_rows), _p(of), t0, t1)
     if rc != 0:
         raise ValueError(f"or_moe_forward failed ({rc})")
-    return Result(dst, a_rows, y_rows, of)
+    return Result(dst, a_rows, y_rows, of, a_f64)
 
 
 def router_topk(logits: np.ndarray, bias: np.ndarray | None, k: int):

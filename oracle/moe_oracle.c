@@ -131,10 +131,12 @@ static int weight_at(const uint8_t *codes, const uint8_t *scales, int64_t K, int
 /* Full fp64 dequantisation of a [rows][K] NVFP4 matrix (tests use it). */
 int or_dequant(const uint8_t *codes, const uint8_t *scales, int64_t rows, int64_t K, double *out) {
   if (K % 16 != 0 || rows < 0) return OR_ERR_ARG;
+  int bad = 0;
+#pragma omp parallel for schedule(static) reduction(| : bad)
   for (int64_t r = 0; r < rows; ++r)
     for (int64_t c = 0; c < K; ++c)
-      if (weight_at(codes, scales, K, r, c, &out[r * K + c]) != OR_OK) return OR_ERR_NAN;
-  return OR_OK;
+      if (weight_at(codes, scales, K, r, c, &out[r * K + c]) != OR_OK) bad = 1;
+  return bad ? OR_ERR_NAN : OR_OK;
 }
 
 /* ---------------------------------------------------------------- routing */
@@ -237,109 +239,135 @@ int64_t or_weighted_row_sum(uint16_t *dst, const double *src, const int32_t *row
 
 /* ------------------------------------------------------ the whole layer */
 
+/* Tokens per block of the layer evaluation below: the intermediates of one
+ * block's pairs are held in memory at once, and each of the three steps of a
+ * block runs its independent output elements in parallel. */
+#define OR_TOKEN_BLOCK 32
+
 /* The MoE expert layer on the plain per-pair definition (see file header).
  * act = 0: relu^2 (gate arrays unused, may be NULL); act = 1: the gated form,
  * gate_codes/gate_scales [E][I][H/2], [E][I][H/16] and gate_global [E].
  * dst [n][H] bf16 is updated in place.  Optional outputs (NULL to skip), all
  * indexed by packed row r = inv[p] from or_routing on the same ids:
- *   a_rows   [R][I] bf16  the intermediate (relu^2 or silu*up) of every kept pair
- *   y_rows   [R][H] fp64  the down-projection of every kept pair
- *   out_f64  [n][H] fp64  dst + sum_j w y before the final rounding
+ *   a_rows     [R][I] bf16  the intermediate (relu^2 or silu*up) of every kept pair
+ *   a_rows_f64 [R][I] fp64  the same intermediate before its bf16 rounding
+ *   y_rows     [R][H] fp64  the down-projection of every kept pair
+ *   out_f64    [n][H] fp64  dst + sum_j w y before the final rounding
  * tok_begin/tok_end restrict the work to a token range (for bounded samples);
- * pass 0 and n for all tokens.  Returns 0, or < 0 on a bad argument / NaN scale. */
+ * pass 0 and n for all tokens.  Returns 0, or < 0 on a bad argument / NaN scale.
+ *
+ * Evaluation order: tokens in blocks of OR_TOKEN_BLOCK; within a block, first
+ * every (pair, intermediate feature) value, then every (pair, output column)
+ * down value, then every (token, column) weighted sum.  Each value is one
+ * plain loop in the order the formulas give (ascending c for the up and gate
+ * sums, ascending i for the down sum, j = 0..k-1 onto dst), so running the
+ * independent values on several threads changes no result. */
 int or_moe_forward_act(int64_t n, int H, int I, int E, int k, const uint16_t *x, const int32_t *ids,
                        const float *topk_w, const uint8_t *up_codes, const uint8_t *up_scales,
                        const uint8_t *dn_codes, const uint8_t *dn_scales, const float *up_global,
                        const float *dn_global, int act, const uint8_t *gate_codes, const uint8_t *gate_scales,
-                       const float *gate_global, uint16_t *dst, uint16_t *a_rows, double *y_rows,
-                       double *out_f64, int64_t tok_begin, int64_t tok_end) {
+                       const float *gate_global, uint16_t *dst, uint16_t *a_rows, double *a_rows_f64,
+                       double *y_rows, double *out_f64, int64_t tok_begin, int64_t tok_end) {
   if (n < 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0 || H % 32 || I % 32) return OR_ERR_ARG;
   if (act != 0 && act != 1) return OR_ERR_ARG;
   if (act == 1 && (!gate_codes || !gate_scales || !gate_global)) return OR_ERR_ARG;
   if (tok_begin < 0 || tok_end > n || tok_begin > tok_end) return OR_ERR_ARG;
   int64_t R = n * (int64_t)k;
   int32_t *inv = NULL;
-  if (a_rows || y_rows) {
+  if (a_rows || a_rows_f64 || y_rows) {
     int32_t *counts = (int32_t *)malloc(sizeof(int32_t) * (size_t)E);
     int32_t *offsets = (int32_t *)malloc(sizeof(int32_t) * (size_t)(E + 1));
     int32_t *perm = (int32_t *)malloc(sizeof(int32_t) * (size_t)(R > 0 ? R : 1));
     inv = (int32_t *)malloc(sizeof(int32_t) * (size_t)(R > 0 ? R : 1));
-    if (!counts || !offsets || !perm || !inv) return OR_ERR_NOMEM;
+    if (!counts || !offsets || !perm || !inv) {
+      free(counts); free(offsets); free(perm); free(inv);
+      return OR_ERR_NOMEM;
+    }
     or_routing(ids, n, k, E, counts, offsets, perm, inv);
     free(counts); free(offsets); free(perm);
   }
   const int64_t up_mat = (int64_t)I * H; /* elements per expert matrix */
+  const int64_t bp = (int64_t)OR_TOKEN_BLOCK * k; /* pairs per block, at most */
+  double *a = (double *)malloc(sizeof(double) * (size_t)(bp * I)); /* [pair of block][i] */
+  double *y = (double *)malloc(sizeof(double) * (size_t)(bp * H)); /* [pair of block][c] */
+  if (!a || !y) {
+    free(a); free(y); free(inv);
+    return OR_ERR_NOMEM;
+  }
   int bad = 0;
-#pragma omp parallel reduction(| : bad)
-  {
-    double *a = (double *)malloc(sizeof(double) * (size_t)I);
-    double *y = (double *)malloc(sizeof(double) * (size_t)H);
-    double *acc = (double *)malloc(sizeof(double) * (size_t)H);
-    double *xd = (double *)malloc(sizeof(double) * (size_t)H);
-    if (!a || !y || !acc || !xd) bad = 1;
-#pragma omp for schedule(dynamic, 1)
-    for (int64_t t = tok_begin; t < tok_end; ++t) {
-      if (!a || !y || !acc || !xd) continue;
+  for (int64_t t0 = tok_begin; t0 < tok_end; t0 += OR_TOKEN_BLOCK) {
+    const int64_t t1 = t0 + OR_TOKEN_BLOCK < tok_end ? t0 + OR_TOKEN_BLOCK : tok_end;
+    const int64_t np = (t1 - t0) * k; /* pairs of this block: p = t0*k + q */
+    /* up projection and the activation, one bf16 rounding per value */
+#pragma omp parallel for schedule(dynamic, 8) reduction(| : bad)
+    for (int64_t qi = 0; qi < np * I; ++qi) {
+      const int64_t q = qi / I, p = t0 * k + q;
+      const int i = (int)(qi % I);
+      const int64_t t = p / k;
+      int32_t e = ids[p];
+      if (e < 0 || e >= E) continue; /* dropped pair */
+      const uint8_t *uc = up_codes + (int64_t)e * (up_mat / 2);
+      const uint8_t *us = up_scales + (int64_t)e * (up_mat / 16);
+      double h = 0.0, w;
       for (int c = 0; c < H; ++c) {
-        xd[c] = or_bf16_to_double(x[t * H + c]);
-        acc[c] = or_bf16_to_double(dst[t * H + c]);
+        if (weight_at(uc, us, H, i, c, &w) != OR_OK) { bad = 1; w = 0.0; }
+        h += w * or_bf16_to_double(x[t * H + c]);
       }
+      h *= (double)up_global[e];
+      double av;
+      if (act == 0) {
+        double r = h > 0.0 ? h : 0.0;
+        av = r * r;
+      } else {
+        const uint8_t *gc = gate_codes + (int64_t)e * (up_mat / 2);
+        const uint8_t *gs = gate_scales + (int64_t)e * (up_mat / 16);
+        double gv = 0.0;
+        for (int c = 0; c < H; ++c) {
+          if (weight_at(gc, gs, H, i, c, &w) != OR_OK) { bad = 1; w = 0.0; }
+          gv += w * or_bf16_to_double(x[t * H + c]);
+        }
+        gv *= (double)gate_global[e];
+        av = gv / (1.0 + exp(-gv)) * h;
+      }
+      uint16_t ab = or_bf16_from_double(av);
+      a[q * I + i] = or_bf16_to_double(ab);
+      if (a_rows) a_rows[(int64_t)inv[p] * I + i] = ab;
+      if (a_rows_f64) a_rows_f64[(int64_t)inv[p] * I + i] = av;
+    }
+    /* down projection of the rounded intermediate */
+#pragma omp parallel for schedule(dynamic, 8) reduction(| : bad)
+    for (int64_t qc = 0; qc < np * H; ++qc) {
+      const int64_t q = qc / H, p = t0 * k + q;
+      const int c = (int)(qc % H);
+      int32_t e = ids[p];
+      if (e < 0 || e >= E) continue; /* dropped pair */
+      const uint8_t *dc = dn_codes + (int64_t)e * (up_mat / 2);
+      const uint8_t *ds = dn_scales + (int64_t)e * (up_mat / 16);
+      double s = 0.0, w;
+      for (int i = 0; i < I; ++i) {
+        if (weight_at(dc, ds, I, c, i, &w) != OR_OK) { bad = 1; w = 0.0; }
+        s += w * a[q * I + i];
+      }
+      y[q * H + c] = s * (double)dn_global[e];
+      if (y_rows) y_rows[(int64_t)inv[p] * H + c] = y[q * H + c];
+    }
+    /* fixed-order weighted sum onto the pre-filled dst, one rounding */
+#pragma omp parallel for schedule(static)
+    for (int64_t tc = 0; tc < (t1 - t0) * H; ++tc) {
+      const int64_t t = t0 + tc / H;
+      const int c = (int)(tc % H);
+      double acc = or_bf16_to_double(dst[t * H + c]);
       for (int j = 0; j < k; ++j) {
         int64_t p = t * k + j;
         int32_t e = ids[p];
         if (e < 0 || e >= E) continue; /* dropped pair */
-        const uint8_t *uc = up_codes + (int64_t)e * (up_mat / 2);
-        const uint8_t *us = up_scales + (int64_t)e * (up_mat / 16);
-        const uint8_t *dc = dn_codes + (int64_t)e * (up_mat / 2);
-        const uint8_t *ds = dn_scales + (int64_t)e * (up_mat / 16);
-        /* up projection and the activation, one bf16 rounding */
-        for (int i = 0; i < I; ++i) {
-          double h = 0.0, w;
-          for (int c = 0; c < H; ++c) {
-            if (weight_at(uc, us, H, i, c, &w) != OR_OK) { bad = 1; w = 0.0; }
-            h += w * xd[c];
-          }
-          h *= (double)up_global[e];
-          double av;
-          if (act == 0) {
-            double r = h > 0.0 ? h : 0.0;
-            av = r * r;
-          } else {
-            const uint8_t *gc = gate_codes + (int64_t)e * (up_mat / 2);
-            const uint8_t *gs = gate_scales + (int64_t)e * (up_mat / 16);
-            double gv = 0.0;
-            for (int c = 0; c < H; ++c) {
-              if (weight_at(gc, gs, H, i, c, &w) != OR_OK) { bad = 1; w = 0.0; }
-              gv += w * xd[c];
-            }
-            gv *= (double)gate_global[e];
-            av = gv / (1.0 + exp(-gv)) * h;
-          }
-          uint16_t ab = or_bf16_from_double(av);
-          a[i] = or_bf16_to_double(ab);
-          if (a_rows) a_rows[(int64_t)inv[p] * I + i] = ab;
-        }
-        /* down projection */
-        for (int c = 0; c < H; ++c) {
-          double s = 0.0, w;
-          for (int i = 0; i < I; ++i) {
-            if (weight_at(dc, ds, I, c, i, &w) != OR_OK) { bad = 1; w = 0.0; }
-            s += w * a[i];
-          }
-          y[c] = s * (double)dn_global[e];
-          if (y_rows) y_rows[(int64_t)inv[p] * H + c] = y[c];
-        }
-        /* fixed-order weighted sum onto the pre-filled dst */
-        for (int c = 0; c < H; ++c) acc[c] += (double)topk_w[p] * y[c];
+        acc += (double)topk_w[p] * y[(p - t0 * k) * H + c];
       }
-      for (int c = 0; c < H; ++c) {
-        if (out_f64) out_f64[t * H + c] = acc[c];
-        dst[t * H + c] = or_bf16_from_double(acc[c]);
-      }
+      if (out_f64) out_f64[t * H + c] = acc;
+      dst[t * H + c] = or_bf16_from_double(acc);
     }
-    free(a); free(y); free(acc); free(xd);
   }
-  free(inv);
+  free(a); free(y); free(inv);
   return bad ? OR_ERR_NAN : OR_OK;
 }
 
@@ -347,10 +375,11 @@ int or_moe_forward_act(int64_t n, int H, int I, int E, int k, const uint16_t *x,
 int or_moe_forward(int64_t n, int H, int I, int E, int k, const uint16_t *x, const int32_t *ids,
                    const float *topk_w, const uint8_t *up_codes, const uint8_t *up_scales,
                    const uint8_t *dn_codes, const uint8_t *dn_scales, const float *up_global,
-                   const float *dn_global, uint16_t *dst, uint16_t *a_rows, double *y_rows,
+                   const float *dn_global, uint16_t *dst, uint16_t *a_rows, double *a_rows_f64, double *y_rows,
                    double *out_f64, int64_t tok_begin, int64_t tok_end) {
   return or_moe_forward_act(n, H, I, E, k, x, ids, topk_w, up_codes, up_scales, dn_codes, dn_scales, up_global,
-                            dn_global, 0, NULL, NULL, NULL, dst, a_rows, y_rows, out_f64, tok_begin, tok_end);
+                            dn_global, 0, NULL, NULL, NULL, dst, a_rows, a_rows_f64, y_rows, out_f64, tok_begin,
+                            tok_end);
 }
 
 /* The router that produces the layer's input (the step before the path; the

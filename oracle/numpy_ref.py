@@ -75,7 +75,7 @@ def moe_dense_masked(wl) -> dict:
 
     Returns the unrounded fp64 output, its bf16 rounding, and per-(token,
     expert) intermediates (relu^2, or g * logistic(g) * u for a workload with
-    gate weights).
+    gate weights), rounded to bf16 ("a") and before that rounding ("a_f64").
     """
     n, H, I, E, k = wl.n, wl.H, wl.I, wl.E, wl.k
     X = bf16_bits_to_f64(wl.x)
@@ -86,7 +86,7 @@ def moe_dense_masked(wl) -> dict:
             e = int(wl.topk_ids[t, j])
             if 0 <= e < E:
                 mask_w[t, e] += float(wl.topk_weights[t, j])
-    a_all = {}
+    a_all, a_raw = {}, {}
     for e in range(E):
         Wu = dequant(wl.up_codes[e], wl.up_scales[e])  # [I, H]
         Wd = dequant(wl.down_codes[e], wl.down_scales[e])  # [H, I]
@@ -94,13 +94,14 @@ def moe_dense_masked(wl) -> dict:
         if getattr(wl, "gate_codes", None) is not None:
             Wg = dequant(wl.gate_codes[e], wl.gate_scales[e])
             gt = (X @ Wg.T) * float(wl.gate_global[e])
-            a = bf16_round(gt * expit(gt) * h)
+            a_raw[e] = gt * expit(gt) * h
         else:
-            a = bf16_round(np.maximum(h, 0.0) ** 2)
+            a_raw[e] = np.maximum(h, 0.0) ** 2
+        a = bf16_round(a_raw[e])
         y = (a @ Wd.T) * float(wl.down_global[e])  # [n, H]
         out += mask_w[:, e:e + 1] * y
         a_all[e] = a
-    return {"out_f64": out, "dst": f64_to_bf16_bits(bf16_round(out)), "a": a_all}
+    return {"out_f64": out, "dst": f64_to_bf16_bits(bf16_round(out)), "a": a_all, "a_f64": a_raw}
 
 
 def matvec_chain(x_bf16: np.ndarray, up_codes, up_scales, dn_codes, dn_scales, g_up: float, g_dn: float):

@@ -91,6 +91,31 @@ def test_create_validates_shapes_first(lib):
                                          None) == 1
 
 
+def test_noalloc_rejects_misaligned_pointers_before_any_cuda_call(lib):
+    """Codes, x and dst need 16-byte alignment, scales 2, globals / ids /
+    weights 4: anything else is MOE_ERR_INVALID_ARG, with nothing enqueued
+    (these fake addresses are never dereferenced)."""
+    vp = ctypes.c_void_p
+    c = api.Config(256, 128, 8, 2, 32, 0)
+    good = dict(up_codes=256, up_scales=256, down_codes=256, down_scales=256, up_global=256, down_global=256)
+    fields = [f for f, _ in api.Weights._fields_]
+    for name, bad in [("up_scales", 257), ("down_scales", 259), ("up_global", 258), ("down_global", 262),
+                      ("up_codes", 264), ("down_codes", 260)]:
+        w = api.Weights(*[dict(good, **{name: bad}).get(f) for f in fields])
+        assert lib.moe_nvfp4_forward_noalloc(ctypes.byref(c), ctypes.byref(w), vp(256), vp(256), vp(256),
+                                             vp(256), 4, None) == 1, name
+    w = api.Weights(*[good.get(f) for f in fields])
+    for args in [(vp(256), vp(258), vp(256), vp(256)),   # ids not 4-byte aligned
+                 (vp(256), vp(256), vp(254), vp(256)),   # weights not 4-byte aligned
+                 (vp(264), vp(256), vp(256), vp(256)),   # x not 16-byte aligned
+                 (vp(256), vp(256), vp(256), vp(248))]:  # dst not 16-byte aligned
+        assert lib.moe_nvfp4_forward_noalloc(ctypes.byref(c), ctypes.byref(w), *args, 4, None) == 1
+    cg = api.Config(256, 128, 8, 2, 32, 0, 0, api.ACT_SWIGLU)
+    wg = api.Weights(*[dict(good, gate_codes=256, gate_scales=257, gate_global=256).get(f) for f in fields])
+    assert lib.moe_nvfp4_forward_noalloc(ctypes.byref(cg), ctypes.byref(wg), vp(256), vp(256), vp(256), vp(256),
+                                         4, None) == 1
+
+
 def test_library_is_built_for_sm103a_only():
     assert "arch=compute_103a,code=sm_103a" in " ".join(B.ARCH)
     assert os.path.exists(B.LIB)

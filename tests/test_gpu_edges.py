@@ -28,7 +28,7 @@ def _check(wl, dev, sample=None, **kw):
     layer.close()
     ranges = sample if sample is not None else [(0, wl.n)]
     for t0, t1 in ranges:
-        ref = oracle.moe_forward(wl, tok_range=(t0, t1)).dst
+        ref = oracle.moe_forward(wl, tok_range=(t0, t1), out_f64=True).out_f64
         ok, err, rms = layer_tolerance_check(got[t0:t1], ref[t0:t1])
         assert ok, (t0, t1, err, rms)
 

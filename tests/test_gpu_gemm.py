@@ -89,13 +89,13 @@ def _layer_vs_oracle(wl, dev, T, sample=None):
     got = run_forward(layer, wl, dev)
     assert layer.device_error() == 0
     if sample is None:
-        ref = oracle.moe_forward(wl)
-        ok, err, rms = layer_tolerance_check(got, ref.dst)
+        ref = oracle.moe_forward(wl, out_f64=True)
+        ok, err, rms = layer_tolerance_check(got, ref.out_f64)
         assert ok, (err, rms)
     else:
         for t0, t1 in sample:
-            ref = oracle.moe_forward(wl, tok_range=(t0, t1))
-            ok, err, rms = layer_tolerance_check(got[t0:t1], ref.dst[t0:t1])
+            ref = oracle.moe_forward(wl, tok_range=(t0, t1), out_f64=True)
+            ok, err, rms = layer_tolerance_check(got[t0:t1], ref.out_f64[t0:t1])
             assert ok, (t0, t1, err, rms)
     again = run_forward(layer, wl, dev)
     assert np.array_equal(got, again)
@@ -137,14 +137,14 @@ def test_grouped_gemm_token_tiles_and_ragged_features(dev, n, H, I, E, k, T, see
     layer = make_layer(wl, dev, gemv_max_rows=T, single_max_tokens=-1)
     got = run_forward(layer, wl, dev)
     assert layer.device_error() == 0
-    ref = oracle.moe_forward(wl, intermediates=True)
-    ok, err, rms = layer_tolerance_check(got, ref.dst)
+    ref = oracle.moe_forward(wl, intermediates=True, out_f64=True)
+    ok, err, rms = layer_tolerance_check(got, ref.out_f64)
     assert ok, (err, rms)
     a = torch.empty((wl.R, wl.I), dtype=torch.int16, device=dev)
     y = torch.empty((wl.R, wl.H), dtype=torch.float32, device=dev)
     layer.debug_intermediates(a, y)
     torch.cuda.synchronize()
-    ok_a, ea, ra = layer_tolerance_check(a.cpu().numpy().view(np.uint16), ref.a_rows)
+    ok_a, ea, ra = layer_tolerance_check(a.cpu().numpy().view(np.uint16), ref.a_f64)
     assert ok_a, ("relu^2 rows", ea, ra)
     ok_y, ey, ry = fp_tolerance_check(y.cpu().numpy(), ref.y_rows)
     assert ok_y, ("down rows", ey, ry)

@@ -51,7 +51,7 @@ def _run_shared(wl, dev):
 def test_shared_expert_matches_oracle(dev, n, H, I, gated, seed):
     wl = _shared(n, H, I, seed, gated)
     got = _run_shared(wl, dev)
-    ref = oracle.moe_forward(wl).dst
+    ref = oracle.moe_forward(wl, out_f64=True).out_f64
     ok, err, rms = layer_tolerance_check(got, ref)
     assert ok, (err, rms)
 
@@ -64,7 +64,7 @@ def test_shared_expert_prefill_4314_sampled(dev):
                     np.zeros((base.n, base.H), np.uint16))
     got = _run_shared(wl, dev)
     for t0, t1 in [(0, 16), (2000, 2010), (4306, 4314)]:
-        ref = oracle.moe_forward(wl, tok_range=(t0, t1)).dst
+        ref = oracle.moe_forward(wl, tok_range=(t0, t1), out_f64=True).out_f64
         ok, err, rms = layer_tolerance_check(got[t0:t1], ref[t0:t1])
         assert ok, (t0, err, rms)
 
@@ -77,15 +77,21 @@ def test_shared_then_routed_in_one_graph(dev, name):
     routed = W.generate(name)
     sh = _shared(routed.n, routed.H, routed.I, seed=95)
     sh.x = routed.x
-    # oracle composition
-    dst0 = oracle.moe_forward(sh).dst
-    comp = W.generate(name)
-    comp.dst = dst0
-    ref = oracle.moe_forward(comp).dst
-
     shared_layer = make_layer(sh, dev)
     routed_layer = make_layer(routed, dev)
     x = to_dev(routed.x, dev)
+    # the shared stage on its own first: against the oracle, and its bits
+    # (deterministic, the same inside the graph) pre-fill the oracle's routed stage
+    stage1 = to_dev(np.zeros((routed.n, routed.H), np.uint16), dev)
+    shared_layer.shared_expert_forward(x, stage1)
+    torch.cuda.synchronize()
+    dst0 = bf16_from_dev(stage1)
+    ok0, err0, rms0 = layer_tolerance_check(dst0, oracle.moe_forward(sh, out_f64=True).out_f64)
+    assert ok0, ("shared stage", err0, rms0)
+    comp = W.generate(name)
+    comp.dst = dst0
+    ref = oracle.moe_forward(comp, out_f64=True).out_f64
+
     ids, tw = to_dev(routed.topk_ids, dev), to_dev(routed.topk_weights, dev)
     dst = to_dev(np.zeros((routed.n, routed.H), np.uint16), dev)
     stream = torch.cuda.Stream(device=dev)

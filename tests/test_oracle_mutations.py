@@ -62,20 +62,20 @@ MUTATIONS = [
      "double mag = (e == 0) ? 1.0 * (double)m : ldexp(1.0 + 0.5 * (double)m, (int)e - 1);",
      [pins.test_e2m1_matches_ocp_table]),
     ("dst_not_added",
-     "        acc[c] = or_bf16_to_double(dst[t * H + c]);",
-     "        acc[c] = 0.0;",
+     "      double acc = or_bf16_to_double(dst[t * H + c]);",
+     "      double acc = 0.0;",
      [pins.test_single_pair_reduces_to_two_matvecs]),
     ("routing_weight_ignored",
-     "for (int c = 0; c < H; ++c) acc[c] += (double)topk_w[p] * y[c];",
-     "for (int c = 0; c < H; ++c) acc[c] += y[c];",
+     "acc += (double)topk_w[p] * y[(p - t0 * k) * H + c];",
+     "acc += y[(p - t0 * k) * H + c];",
      [lambda: pins.test_gather_equals_dense_masked(("tiny",))]),
     ("up_global_missing",
-     "          h *= (double)up_global[e];",
-     "          h *= 1.0;",
+     "      h *= (double)up_global[e];",
+     "      h *= 1.0;",
      [lambda: pins.test_gather_equals_dense_masked(("tiny",))]),
     ("relu_dropped_in_layer",
-     "            double r = h > 0.0 ? h : 0.0;\n            av = r * r;",
-     "            double r = h;\n            av = r * r;",
+     "        double r = h > 0.0 ? h : 0.0;\n        av = r * r;",
+     "        double r = h;\n        av = r * r;",
      [pins.test_all_negative_preactivations_leave_dst_unchanged]),
     ("router_ties_to_higher_index",
      "        if (best < 0 || z > best_z) {",

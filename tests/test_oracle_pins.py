@@ -323,6 +323,11 @@ def test_gather_equals_dense_masked(shape):
     for r, p in enumerate(perm):
         t, e = p // wl.k, int(wl.topk_ids.ravel()[p])
         assert np.array_equal(numpy_ref.bf16_bits_to_f64(res.a_rows[r]), dense["a"][e][t])
+        # the unrounded intermediate: the restatement's value up to fp64 summation order,
+        # and the bf16 row is its one rounding
+        raw = dense["a_f64"][e][t]
+        assert np.allclose(res.a_f64[r], raw, rtol=1e-12, atol=1e-12 * max(np.abs(raw).max(), 1e-300))
+        assert np.array_equal(numpy_ref.bf16_round(res.a_f64[r]), numpy_ref.bf16_bits_to_f64(res.a_rows[r]))
 
 
 def test_duplicate_expert_in_one_token():

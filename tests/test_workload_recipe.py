@@ -69,3 +69,29 @@ def test_bias_skews_expert_counts():
     unbiased = np.bincount(W.make_routing(4314, 128, 6, 0.0, seed=5)[0].ravel(), minlength=128)
     assert skewed.sum() == unbiased.sum() == 4314 * 6
     assert skewed.std() > 3 * unbiased.std()
+
+
+def test_full_contract_scale_draws():
+    """'full' draws every finite E4M3FN byte (both signs, zero, subnormals) and
+    never a NaN byte; 'low' draws exactly the bytes with exponent field 0..3."""
+    rng = np.random.Generator(np.random.PCG64(3))
+    full = W.draw_scales(rng, (200000,), "full")
+    seen = set(np.unique(full).tolist())
+    assert seen == set(range(256)) - {0x7F, 0xFF}
+    low = W.draw_scales(rng, (50000,), "low")
+    want = {(s << 7) | (e << 3) | m for s in (0, 1) for e in range(4) for m in range(8)}
+    assert set(np.unique(low).tolist()) == want
+    assert np.any(low & 0x80) and np.any((low & 0x78) == 0)  # negative and subnormal scales occur
+
+
+def test_distinct_globals_and_unchanged_shared_draws():
+    base = W.small_custom(6, 64, 32, 5, 2, seed=9)
+    wide = W.small_custom(6, 64, 32, 5, 2, seed=9, globals_="distinct", gated=True)
+    for g in (wide.up_global, wide.down_global, wide.gate_global):
+        m, _ = np.frexp(g.astype(np.float64))
+        assert not np.any(m == 0.5), "a global is a power of two"
+    allg = np.concatenate([wide.up_global, wide.down_global, wide.gate_global])
+    assert len(np.unique(allg)) == allg.size
+    # the globals are drawn last: codes, scales, routing and activations are the recipe's
+    for name in ("x", "topk_ids", "topk_weights", "up_codes", "up_scales", "down_codes", "down_scales", "dst"):
+        assert np.array_equal(getattr(base, name), getattr(wide, name)), name
