@@ -16,6 +16,13 @@ Multi-GPU (torchrun): the layer does not shard across GPUs here, so every
 rank runs an independent replica on its own GPU (weak scaling, no data-path
 collective); rank 0 reports max-over-ranks time and the summed throughput.
 
+The metric covers decode and prefill, so the same run also measures the
+workloads named by --workloads (default decode-32, prefill-4314 and
+prefill-16384; prefill with fewer steps) and reports each under "workloads"
+with its own tokens/s, roofline (HBM for the streaming kernel, bf16 tensor
+peak for the grouped GEMMs, plus the layer's expert flops over its step time
+for prefill), end-to-end host-buffer number, clocks and oracle sample.
+
 --impl reference times the fp64 CPU oracle (the only other implementation of
 the layer) on the host cores, on a bounded sample of the same workload.
 """
@@ -55,6 +62,9 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--gated", action="store_true",
                    help="gated experts (silu(gate) * up) on the same workload shapes, gate weights drawn last")
+    p.add_argument("--workloads", default="decode-32,prefill-4314,prefill-16384",
+                   help="other workloads measured in the same run and reported under 'workloads' "
+                        "(comma-separated; 'none' for the headline workload only)")
     return p.parse_args()
 
 
@@ -111,9 +121,17 @@ def algorithmic_work(wl, ids_list, T):
         out["small_experts"] = (out["gemv_up"][0] + out["gemv_down"][0], out["gemv_up"][1] + out["gemv_down"][1])
         del out["gemv_up"], out["gemv_down"]
     if single:
-        # the whole layer is one kernel: its bytes are those of the four steps it fuses
-        parts = ("routing", "gemv_up", "gemv_down", "combine")
-        out = {"decode": (sum(out[p][0] for p in parts), sum(out[p][1] for p in parts))}
+        # the whole layer is one kernel: the layer's algorithmic bytes -- the
+        # NVFP4 weights of every touched expert read once, x read, dst read and
+        # written, ids and weights read (8 B per pair); the intermediates stay
+        # on chip or in L2 and are not counted
+        w_bytes = 0.0
+        for ids in ids_list:
+            c = np.bincount(ids.ravel(), minlength=E)
+            w_bytes += float(np.count_nonzero(c)) * (up_mats + 1) * mat_bytes
+        b = w_bytes / m + 3.0 * n * H * 2 + 8.0 * n * k
+        flops = sum(out[p][1] for p in ("gemv_up", "gemv_down"))
+        out = {"decode": (b, flops)}
     return out
 
 
@@ -203,7 +221,13 @@ class ClockSampler:
 
 # ----------------------------------------------------------------- CPU baseline
 def cpu_baseline(wl, seconds: float):
-    """The fp64 oracle as it stands, on this host's cores, on a bounded token sample."""
+    """The fp64 oracle as it stands, on this host's cores, on a bounded sample.
+
+    The oracle runs the independent values of each step (one intermediate
+    feature of one pair, one output column of one pair, one output element)
+    in parallel on all of its threads, so a one-token batch uses every core
+    too.  Batches of at most 64 tokens run whole, repeated for about
+    `seconds`; larger ones on a contiguous token range grown to about that."""
     import oracle
 
     n_threads = oracle.num_threads()
@@ -218,10 +242,8 @@ def cpu_baseline(wl, seconds: float):
         dt = time.perf_counter() - t0
         toks = runs * wl.n
         sample = f"whole workload ({wl.n} tokens) x {runs} runs"
-        cores = min(n_threads, wl.n)
     else:
-        # grow a contiguous token range until the run takes about `seconds`
-        t1 = max(1, min(wl.n, n_threads))
+        t1 = max(1, min(wl.n, 8))
         while True:
             t0 = time.perf_counter()
             oracle.moe_forward(wl, tok_range=(0, t1))
@@ -231,8 +253,7 @@ def cpu_baseline(wl, seconds: float):
             t1 = min(wl.n, max(t1 * 2, int(t1 * seconds / max(dt, 1e-3) * 0.7)))
         toks = t1
         sample = f"tokens [0, {t1}) of {wl.n}"
-        cores = min(n_threads, t1)
-    return {"value": toks / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample,
+    return {"value": toks / dt, "unit": "tokens/s", "cores": n_threads, "kind": "oracle", "sample": sample,
             "seconds": dt}
 
 
@@ -285,24 +306,23 @@ def replica_throughput(ms_local: float, tokens_per_rank: int, dist=None, device=
     return ms, world * tokens_per_rank / (ms / 1000.0)
 
 
-def run_ours(args):
-    import torch
+def _launches_per_step(n, k, T):
+    """Kernels one forward enqueues: the single launch; or routing (one kernel,
+    or two above 4096 pairs), gather, small experts, 2 GEMMs, combine; or
+    routing, 2 GEMVs, combine."""
+    if decode_single_launch(n, k, T):
+        return 1
+    routing_launches = 1 if n * k <= 4096 else 2
+    return routing_launches + (5 if n > T else 3)
 
-    from nvfp4_quantized_moe_topk_gb300 import api
 
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    dev = torch.device(f"cuda:{local}")
-    torch.cuda.set_device(dev)
-    api.load(build_if_missing=True)
-    cfg = W.CONFIGS[args.workload]
-    wl = W.generate(args.workload, gated=args.gated)
+def bench_workload(api, torch, name, args, dev, *, steps, warmup, cpu_seconds, dist=None, local=0):
+    """Measure one workload: the timed forward steps, the per-kernel roofline,
+    the router, the end-to-end host-buffer call and (optionally) the oracle
+    on the host cores.  Returns the fields of one result record."""
+    world = dist.get_world_size() if dist is not None else 1
+    cfg = W.CONFIGS[name]
+    wl = W.generate(name, gated=args.gated)
     T = args.gemv_max_rows if args.gemv_max_rows > 0 else 8
     routings = [(wl.topk_ids, wl.topk_weights)] + [
         W.make_routing(wl.n, wl.E, wl.k, cfg["bias_sigma"], seed=5000 + 97 * i) for i in range(1, N_ROUTINGS)]
@@ -376,9 +396,9 @@ def run_ours(args):
         if t_graph < t_direct:
             graphs = kept
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     with torch.cuda.stream(stream):
-        for i in range(args.warmup):
+        for i in range(warmup):
             flush.fill_(float(i))
             step(i)
         torch.cuda.synchronize()
@@ -387,7 +407,7 @@ def run_ours(args):
         torch.cuda.synchronize()
         with ClockSampler(local) as clk:
             t_wall = time.perf_counter()
-            for i in range(args.steps):
+            for i in range(steps):
                 flush.fill_(float(i))
                 ev[i][0].record(stream)
                 step(i)
@@ -404,7 +424,7 @@ def run_ours(args):
     layer.set_timing(True)
     layer.kernel_times()
     with torch.cuda.stream(stream):
-        for i in range(args.steps):
+        for i in range(steps):
             flush.fill_(float(i))
             fwd(i)
         torch.cuda.synchronize()
@@ -413,22 +433,39 @@ def run_ours(args):
     per_launch_ms = {kname: tot / cnt for kname, (tot, cnt) in kt.items() if cnt}
     work = algorithmic_work(wl, [r[0] for r in routings], T)
     peaks = load_peaks()
+
+    def roofline_of(kname):
+        b_alg, f_alg = work.get(kname, (0.0, 0.0))
+        t = per_launch_ms[kname] / 1000.0
+        if kname.startswith("gemm"):
+            ach = f_alg / t / 1e12
+            r = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                 "frac": ach / peaks["bf16_tflops"]}
+        else:
+            ach = b_alg / t / 1e9
+            r = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                 "frac": ach / peaks["hbm_gbs"]}
+        r["traffic"] = profiled_traffic(name + ("+gated" if args.gated else ""), kname)
+        r["kernel"] = kname
+        r["kernel_ms"] = per_launch_ms[kname]
+        r["peak_source"] = peaks["source"]
+        return r
+
     dom = max(per_launch_ms, key=lambda kname: per_launch_ms[kname])
-    b_alg, f_alg = work.get(dom, (0.0, 0.0))
-    if dom.startswith("gemm"):
-        achieved = f_alg / (per_launch_ms[dom] / 1000.0) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": achieved / peaks["bf16_tflops"], "traffic": None}
-    else:
-        achieved = b_alg / (per_launch_ms[dom] / 1000.0) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "traffic": None}
-    roof["traffic"] = profiled_traffic(args.workload + ("+gated" if args.gated else ""), dom)
-    roof["kernel"] = dom
-    roof["kernel_ms"] = per_launch_ms[dom]
-    roof["peak_source"] = peaks["source"]
+    roof = roofline_of(dom)
     layer_bytes = sum(b for kname, (b, f) in work.items())
     layer_flops = sum(f for kname, (b, f) in work.items() if kname.startswith("gemm"))
+    layer_rec = {"alg_bytes": layer_bytes, "alg_gemm_flops": layer_flops,
+                 "hbm_frac_whole_layer": layer_bytes / (ms / 1000.0) / 1e9 / peaks["hbm_gbs"],
+                 "per_kernel_ms": per_launch_ms}
+    if any(kname.startswith("gemm") for kname in per_launch_ms):
+        # the prefill figure of merit: all the layer's expert flops (4 R H I, routed rows only,
+        # gated 6 R H I) over the whole layer's step time, against the bf16 peak
+        f_layer = (6.0 if wl.gated else 4.0) * wl.n * wl.k * wl.H * wl.I
+        layer_rec["layer_tflops"] = f_layer / (ms / 1000.0) / 1e12
+        layer_rec["layer_tensor_frac"] = layer_rec["layer_tflops"] / peaks["bf16_tflops"]
+        layer_rec["gemm_rooflines"] = {kname: roofline_of(kname) for kname in per_launch_ms
+                                       if kname.startswith("gemm")}
 
     # the router that produces the layer's routing (timed on its own, same shapes)
     router = None
@@ -442,7 +479,7 @@ def run_ours(args):
         r_counts = torch.empty(wl.E, dtype=torch.int32, device=dev)
         r_ms = []
         with torch.cuda.stream(stream):
-            for i in range(3 + max(args.steps, 10)):
+            for i in range(3 + max(steps, 10)):
                 flush.fill_(float(i))
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
@@ -464,7 +501,7 @@ def run_ours(args):
     wh = [torch.from_numpy(r[1]).pin_memory() for r in routings]
     for i in range(3):
         layer.forward_host(xh, ih[i % N_ROUTINGS], wh[i % N_ROUTINGS], dh, stream=stream)
-    e2e_steps = max(args.steps, 10)
+    e2e_steps = max(steps, 10)
     # wall time of the synchronous host-buffer call only (the L2 flush runs outside it)
     tot = 0.0
     for i in range(e2e_steps):
@@ -477,34 +514,72 @@ def run_ours(args):
     h2d = wl.n * wl.H * 2 * 2 + wl.n * wl.k * 8
     d2h = wl.n * wl.H * 2
     layer.close()
+    used_graph = graphs is not None
+    del layer, x, dst, ids_d, w_d, flush, graphs
+    torch.cuda.empty_cache()
 
-    clocks = clk.summary()
-    # single launch; or routing (one kernel, or two above 4096 pairs), gather, small experts, 2 GEMMs,
-    # combine; or routing, 2 GEMVs, combine
-    routing_launches = 1 if wl.n * wl.k <= 4096 else 2
-    launches_per_step = 1 if decode_single_launch(wl.n, wl.k, T) else routing_launches + (5 if wl.n > T else 3)
-    line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, random NVFP4 weights)",
-        "config": {"workload": args.workload, "activation": "swiglu" if args.gated else "relu2",
+    rec = {
+        "value": value, "unit": "tokens/s", "ms_per_step": ms, "steps": steps, "warmup": warmup,
+        "config": {"workload": name, "activation": "swiglu" if args.gated else "relu2",
                    "n": wl.n, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
                    "gemv_max_rows": T, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "flushed before every step (256 MB write)", "routings": N_ROUTINGS,
-                   "graph": graphs is not None},
+                   "graph": used_graph},
         "roofline": roof,
-        "layer": {"alg_bytes": layer_bytes, "alg_gemm_flops": layer_flops,
-                  "hbm_frac_whole_layer": layer_bytes / (ms / 1000.0) / 1e9 / peaks["hbm_gbs"],
-                  "per_kernel_ms": per_launch_ms},
-        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+        "layer": layer_rec,
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "router": router,
-        "gpu_launches": launches_per_step * args.steps,
-        "clocks": clocks,
+        "gpu_launches": _launches_per_step(wl.n, wl.k, T) * steps,
+        "clocks": clk.summary(),
         "wall_s_timed_region": t_wall,
     }
-    if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+    rank = dist.get_rank() if dist is not None else 0
+    if rank == 0 and cpu_seconds > 0:
+        rec["cpu_baseline"] = cpu_baseline(wl, cpu_seconds)
+    return rec
+
+
+def run_ours(args):
+    import torch
+
+    from nvfp4_quantized_moe_topk_gb300 import api
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    api.load(build_if_missing=True)
+    head = bench_workload(api, torch, args.workload, args, dev, steps=args.steps, warmup=args.warmup,
+                          cpu_seconds=0.0 if args.no_cpu_baseline else args.cpu_seconds, dist=dist, local=local)
+    # The metric covers decode and prefill: the other workloads are measured in
+    # the same run, each with its own steps, roofline, end-to-end call and
+    # oracle sample (prefill takes fewer steps: milliseconds each).
+    extras = {}
+    names = [] if args.workloads.strip() in ("", "none") else [w.strip() for w in args.workloads.split(",")]
+    for nm in names:
+        if nm == args.workload or nm not in W.CONFIGS:
+            continue
+        steps = args.steps if W.CONFIGS[nm]["n"] <= 64 else max(5, min(args.steps, 20))
+        extras[nm] = bench_workload(api, torch, nm, args, dev, steps=steps, warmup=max(3, args.warmup),
+                                    cpu_seconds=0.0 if args.no_cpu_baseline else 3.0, dist=dist, local=local)
+    line = {
+        "metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, random NVFP4 weights)",
+        "config": head["config"], "roofline": head["roofline"], "layer": head["layer"], "e2e": head["e2e"],
+        "router": head["router"], "gpu_launches": head["gpu_launches"], "clocks": head["clocks"],
+        "wall_s_timed_region": head["wall_s_timed_region"],
+    }
+    if "cpu_baseline" in head:
+        line["cpu_baseline"] = head["cpu_baseline"]
+    if extras:
+        line["workloads"] = extras
     if dist:
         dist.barrier()
         dist.destroy_process_group()

@@ -41,6 +41,19 @@ def test_work_model_gated_up_reads_two_matrices():
     assert gated["small_experts"][0] == plain["small_experts"][0] + mat
 
 
+def test_work_model_single_launch_counts_only_the_layer_bytes():
+    """A batch run as one launch: the touched experts' weights once, x read,
+    dst read and written, 8 B of ids and weights per pair -- no intermediates."""
+    n, H, I, E, k, T = 2, 256, 128, 8, 3, 8
+    ids = np.array([[0, 3, 5], [3, 6, 1]], np.int32)  # five experts touched
+    mat = H * I // 2 + H * I // 16
+    w = bench.algorithmic_work(_wl(n, H, I, E, k), [ids], T)
+    assert set(w) == {"decode"}
+    assert w["decode"][0] == 5 * 2 * mat + 3 * n * H * 2 + 8 * n * k
+    g = bench.algorithmic_work(_wl(n, H, I, E, k, gated=True), [ids], T)
+    assert g["decode"][0] == 5 * 3 * mat + 3 * n * H * 2 + 8 * n * k
+
+
 def _fake_tree(tmp_path, text):
     csrc = tmp_path / "nvfp4_quantized_moe_topk_gb300" / "csrc"
     csrc.mkdir(parents=True)

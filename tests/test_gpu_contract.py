@@ -27,7 +27,9 @@ more than the tolerance), and distinct non-power-of-two globals throughout.
 The bound is the layer's: |y_gpu - y_ref| <= 1e-2 * RMS(y_ref) + 1/2 ulp(y_gpu)
 against the oracle's unrounded fp64 output, the same for the intermediates
 (relu^2 or silu * up rows against their unrounded values), and
-1e-2 * RMS for the fp32 down rows.
+1e-2 * RMS for the fp32 down rows -- the down rows and the output plus the
+intermediate's own rounding difference carried through |W_down| (see
+``_check``).
 
 The last tests show the bound has teeth on these inputs: mistakes a kernel
 could plausibly make (up and down globals swapped, another expert's global,
@@ -42,7 +44,8 @@ import pytest
 
 import oracle
 from nvfp4_quantized_moe_topk_gb300 import workload as W
-from helpers import bf16_from_dev, fp_tolerance_check, layer_tolerance_check, make_layer, run_forward, to_dev
+from helpers import (bf16_from_dev, flip_allowance, fp_tolerance_check, layer_tolerance_check, make_layer,
+                     run_forward, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -68,18 +71,26 @@ def _intermediates(layer, wl, dev):
 
 
 def _check(wl, dev, *, intermediates=True, **layer_kw):
+    """Layer output, intermediates and down rows against the oracle.  With
+    scales over the whole e4m3 range one weight block can dominate a down
+    row, so a one-step rounding difference of the bf16 intermediate (fp32 vs
+    fp64 sums on either side of a boundary, itself within the intermediate's
+    bound) moves that row by more than 1e-2 RMS: the down rows and the output
+    are allowed that propagated difference on top (``flip_allowance``)."""
     layer = make_layer(wl, dev, **layer_kw)
     got = run_forward(layer, wl, dev)
     assert layer.device_error() == 0
     ref = oracle.moe_forward(wl, intermediates=intermediates, out_f64=True)
-    ok, err, rms = layer_tolerance_check(got, ref.out_f64)
-    assert ok, f"layer output: max|err| {err:.4g} vs rms {rms:.4g}"
+    extra_out = None
     if intermediates:
         a, y = _intermediates(layer, wl, dev)
         ok_a, ea, ra = layer_tolerance_check(a, ref.a_f64)
         assert ok_a, f"intermediate rows: max|err| {ea:.4g} vs rms {ra:.4g}"
-        ok_y, ey, ry = fp_tolerance_check(y, ref.y_rows)
+        e_rows, extra_out = flip_allowance(wl, a, ref.a_rows)
+        ok_y, ey, ry = fp_tolerance_check(y, ref.y_rows, extra=e_rows)
         assert ok_y, f"down rows: max|err| {ey:.4g} vs rms {ry:.4g}"
+    ok, err, rms = layer_tolerance_check(got, ref.out_f64, extra=extra_out)
+    assert ok, f"layer output: max|err| {err:.4g} vs rms {rms:.4g}"
     again = run_forward(layer, wl, dev)
     assert np.array_equal(got, again), "repeated forward changed bits"
     layer.close()
@@ -202,9 +213,17 @@ def _sens_workload(label):
     scales = "low" if label.endswith("low") else "full"
     gated = "gated" in label
     if label.startswith("decode-1"):
-        return W.generate("decode-1", gated=gated, scales=scales, globals_="distinct")
-    return W.small_custom(120, 512, 384, 16, 2, seed=66, bias_sigma=1.0, gated=gated, scales=scales,
-                          globals_="distinct")
+        wl = W.generate("decode-1", gated=gated, scales=scales, globals_="distinct")
+    else:
+        wl = W.small_custom(120, 512, 384, 16, 2, seed=66, bias_sigma=1.0, gated=gated, scales=scales,
+                            globals_="distinct")
+    if gated:
+        # Where |g| >> 1 silu(g) is g or 0, so silu(g_gate G) g_up U and
+        # silu(g_up G) g_gate U agree and a swap of the two globals is
+        # invisible there; smaller gate globals put the gate pre-activations
+        # at O(1), where the logistic bends.
+        wl.gate_global = (wl.gate_global * np.float32(2.0 ** (-10 if scales == "full" else -5))).astype(np.float32)
+    return wl
 
 
 @pytest.mark.parametrize("label,kw,mistakes", SENSITIVITY, ids=[s[0] for s in SENSITIVITY])
