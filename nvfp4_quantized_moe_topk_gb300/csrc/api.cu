@@ -34,6 +34,8 @@
 #include <new>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/moe_nvfp4.h"
 #include "kernels.h"
 
@@ -46,6 +48,10 @@ enum KernelId {
 };
 const char* const kKernelNames[kKCount] = {"routing",   "gather",    "gemv_up", "gemm_up",      "gemv_down",
                                            "gemm_down", "combine",   "decode",  "small_experts"};
+// The same names as NVTX ranges (what a profiler shows around each launch).
+const char* const kRangeNames[kKCount] = {"moe_nvfp4/routing",   "moe_nvfp4/gather",  "moe_nvfp4/gemv_up",
+                                          "moe_nvfp4/gemm_up",   "moe_nvfp4/gemv_down", "moe_nvfp4/gemm_down",
+                                          "moe_nvfp4/combine",   "moe_nvfp4/decode",  "moe_nvfp4/small_experts"};
 
 struct TimingSlot {
   cudaEvent_t beg = nullptr, end = nullptr;
@@ -152,12 +158,14 @@ bool is_sm103(int dev) {
   return major == 10 && minor == 3;
 }
 
-// Brackets one kernel launch with timing events when timing is on.
+// Brackets one kernel launch with an NVTX range (a no-op unless a profiler
+// is attached) and, when timing is on, with timing events.
 struct TimedLaunch {
   moe_nvfp4* h;
   cudaStream_t s;
   TimingSlot* slot = nullptr;
   TimedLaunch(moe_nvfp4* h_, cudaStream_t s_, int kernel) : h(h_), s(s_) {
+    nvtxRangePushA(kRangeNames[kernel]);
     if (!h || !h->timing || h->slots.empty()) return;
     slot = &h->slots[h->slot_next];
     h->slot_next = (h->slot_next + 1) % h->slots.size();
@@ -173,6 +181,7 @@ struct TimedLaunch {
   }
   ~TimedLaunch() {
     if (slot) cudaEventRecord(slot->end, s);
+    nvtxRangePop();
   }
 };
 
