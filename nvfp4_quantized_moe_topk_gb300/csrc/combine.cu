@@ -3,8 +3,9 @@
 // gllm pull request #91, "What changes", MoE gather: one row gather fills the
 // packed activation buffer (row r holds the token of pair perm_pair[r]), and
 // one WeightedRowSum adds each token's topK expert outputs onto the pre-filled
-// shared-expert output: dst[i] += sum_j w[i,j] * src[rows[i,j]], the j terms
-// in a fixed order, one thread per output element, no atomics.
+// shared-expert output: dst[i] += sum_j w[i,j] * src[rows[i,j]].  Each
+// element of dst has a single writer that walks j upward, so the sum needs no
+// atomic adds and does not depend on how the threads are scheduled.
 //
 // Here each thread owns 8 consecutive columns of one dst row (one 16-byte bf16
 // vector): it widens dst to fp32, adds w[i][j] * src[rows[i][j]][c] for

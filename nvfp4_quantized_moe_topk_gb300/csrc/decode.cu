@@ -31,7 +31,7 @@
 //   5. one grid barrier (a single arrival per CTA) separates up from down; the
 //      weight chunks of the first down tiles are already in flight across it,
 //      their activation rows (the relu^2 rows) are requested right after it;
-//   6. the WeightedRowSum onto dst (fixed j order, one fma each, no atomics on
+//   6. the WeightedRowSum onto dst (j ascending, one fma each, no atomics on
 //      data): for up to 8 tokens the last warp to finish a 16-column block of
 //      down tiles applies it to those columns, for more tokens every thread
 //      takes one element after a second grid barrier.

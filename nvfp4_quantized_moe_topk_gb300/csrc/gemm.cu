@@ -2,8 +2,9 @@
 //
 // gllm pull request #91 ("perf: gather tokens per MoE expert, run large NVFP4
 // GEMMs on bf16 tensor cores"), section "What changes", bf16 NVFP4 GEMM: past
-// the GEMV threshold the NVFP4 weight is unpacked to bf16 -- exactly, since a
-// code times an e4m3 block scale has at most 6 significant bits -- and fed to
+// the GEMV threshold the NVFP4 weight is unpacked to bf16 -- without rounding:
+// an e2m1 value carries 2 significant bits and an e4m3 scale up to 4, so
+// their product needs no more than bf16's 8 -- and fed to
 // a bf16 tensor-core GEMM whose alpha carries the per-tensor global.  There
 // the unpack is a separate kernel writing a bf16 copy to global memory and the
 // GEMM is a library call; here both live in one persistent kernel and the

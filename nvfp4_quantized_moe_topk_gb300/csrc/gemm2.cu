@@ -1,8 +1,9 @@
 // gemm2.cu -- grouped NVFP4 GEMM for the layer, weights as the tensor-memory operand.
 //
 // gllm pull request #91 ("What changes", bf16 NVFP4 GEMM): above the GEMV
-// threshold the NVFP4 weight is unpacked to bf16 -- exactly, since a code
-// times an e4m3 block scale has at most 6 significant bits -- and multiplied on
+// threshold the NVFP4 weight is unpacked to bf16 -- without rounding, because
+// an e2m1 value (2 significant bits) times an e4m3 scale (up to 4) needs no
+// more than bf16's 8 -- and multiplied on
 // bf16 tensor cores, with the per-tensor global in the GEMM's alpha.  On sm_103a
 // the unpacked weight never needs to touch shared memory: tcgen05.mma can read
 // its A operand from tensor memory, so the unpack warps write the bf16 weights

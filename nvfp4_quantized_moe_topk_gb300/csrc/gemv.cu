@@ -10,7 +10,7 @@
 // from HBM with 128-bit loads, one 16-byte chunk (32 codes) per lane per step,
 // the next row's chunks already in flight while the current one is summed.
 // Codes are unpacked exactly to bf16 (a code-pair lookup times the e4m3 block
-// scale; the product has at most 6 significant bits), multiplied against the
+// scale; 2 + 4 significant bits fit in bf16's 8), multiplied against the
 // bf16 activations with fp32 fused multiply-adds, and reduced across the warp
 // with shuffles in a fixed butterfly order, so results are run-to-run
 // identical.  relu^2 and the bf16 rounding of the up projection are fused
