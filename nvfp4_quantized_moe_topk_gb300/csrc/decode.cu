@@ -166,7 +166,7 @@ __device__ __forceinline__ void all_warps_sync(int nthreads) {
 // 16-row tile rt of expert e (local item i of the phase), for tokens tok0 ..
 // tok0 + 7 of that expert.  Phase 0 is the up projection, phase 1 down, 2 done.
 struct __align__(16) Cur {
-  int32_t ph, i, tok0, kt, kt_end, e, rt, cnt, off, pad0, pad1, pad2;
+  int32_t ph, i, tok0, kt, kt_end, e, rt, cnt, off, srow, pad1, pad2;  // srow: first stage row (staged mode)
 };
 
 __device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
@@ -193,9 +193,18 @@ struct DecodeCtx {
   uint32_t wbytes;          // weight bytes of a ring slot (the activation rows follow)
   int32_t Wu, Wd;           // warps that take part in each phase (split mode)
   int32_t ura, urb, dra, drb;      // this warp's tile range per phase (split mode)
+  // Staged mode: the activation rows of the CTA's experts are copied once per
+  // phase into a CTA-wide stage instead of with every chunk.
+  int32_t staged;
+  uint8_t* stage;
+  uint32_t RSu, RSd;               // stage row stride per phase
+  const int32_t* sbu;              // up: first stage row of staged expert j (span_u + 1 entries)
+  const int32_t* sbd;              // down: the same
+  int32_t elo_u, elo_d, span_u, span_d;  // first staged expert (index into s_act) and count, per phase
 
   __device__ DecodeCtx(const DecodeArgs& args) : a(args) {}
 
+  template <bool S>
   __device__ __forceinline__ void load_item(Cur& c) const {
     const int32_t lo = c.ph ? d_lo : u_lo, NP = c.ph ? NPd : NPu;
     const int32_t flat = lo + c.i;
@@ -204,8 +213,10 @@ struct DecodeCtx {
     c.e = s_act[ei];
     c.cnt = s_counts[c.e];
     c.off = s_off[c.e];
+    if (S) c.srow = (c.ph ? sbd : sbu)[ei - (c.ph ? elo_d : elo_u)];
   }
   // First segment of phase ph or a later one (ph = 2 when the warp is done).
+  template <bool S>
   __device__ __forceinline__ void enter_phase(Cur& c, int32_t ph) const {
     for (; ph < 2; ++ph) {
       c.ph = ph;
@@ -218,19 +229,20 @@ struct DecodeCtx {
           c.i = ra / KT;
           c.kt = ra - c.i * KT;
           c.kt_end = min(KT, rb - c.i * KT);
-          load_item(c);
+          load_item<S>(c);
           return;
         }
       } else if (warp < (ph ? n_dn : n_up)) {
         c.i = warp;
         c.kt = 0;
         c.kt_end = KT;
-        load_item(c);
+        load_item<S>(c);
         return;
       }
     }
     c.ph = 2;
   }
+  template <bool S>
   __device__ __forceinline__ void advance(Cur& c) const {
     c.kt += kDecCK;
     if (c.kt < c.kt_end) return;
@@ -241,7 +253,7 @@ struct DecodeCtx {
       if (c.i * KT < rb) {
         c.kt = 0;
         c.kt_end = min(KT, rb - c.i * KT);
-        load_item(c);
+        load_item<S>(c);
         return;
       }
     } else {
@@ -254,11 +266,11 @@ struct DecodeCtx {
       c.i += W;
       if (c.i < (c.ph ? n_dn : n_up)) {
         c.kt = 0;
-        load_item(c);
+        load_item<S>(c);
         return;
       }
     }
-    enter_phase(c, c.ph + 1);
+    enter_phase<S>(c, c.ph + 1);
   }
   __device__ __forceinline__ const uint8_t* chunk_src(const Cur& c) const {
     const int32_t KT = c.ph ? KTd : KTu, NT = c.ph ? NTd : NTu;
@@ -273,11 +285,12 @@ struct DecodeCtx {
   // the activation rows, the latter possibly issued later) and bulk-copy the
   // weight tiles: row tile rt into the slot's first half, rt + 1 (the next
   // KT tiles in memory) into the second.
+  template <bool S>
   __device__ __forceinline__ void issue_weights(const Cur& c, uint8_t* slot, uint64_t* bar, uint64_t pol) const {
     const uint32_t n_kt = (uint32_t)kts(c);
     const uint32_t nt = (uint32_t)min(kDecPassTok, c.cnt - c.tok0);
     const bool pair = two(c);
-    mbar_arrive_expect_tx(bar, n_kt * ((pair ? 2u : 1u) * kTileBytes + nt * 128u));
+    mbar_arrive_expect_tx(bar, n_kt * ((pair ? 2u : 1u) * kTileBytes + (S ? 0u : nt * 128u)));
     const uint8_t* src = chunk_src(c);
     bulk_g2s_hint(slot, src, n_kt * kTileBytes, bar, pol);
     if (pair)
@@ -286,7 +299,9 @@ struct DecodeCtx {
   }
   // Lanes g < nt: bulk-copy token column g's activation row segment (kts x 64
   // bf16) into the slot; it completes on the slot's barrier.
+  template <bool S>
   __device__ __forceinline__ void issue_acts(const Cur& c, int lane, uint8_t* slot, uint64_t* bar) const {
+    if (S) return;
     const int32_t nt = min(kDecPassTok, c.cnt - c.tok0);
     if (lane < nt) {
       const int32_t pr = c.off + c.tok0 + lane;
@@ -300,7 +315,108 @@ struct DecodeCtx {
       bulk_g2s(slot + wbytes + lane * kDecActRow, src, (uint32_t)kts(c) * 128u, bar);
     }
   }
+  // Lanes of one warp: copy the activation rows of phase ph's staged experts
+  // into the stage (expert j's rows from stage row sb[j] on, one bulk copy
+  // each) after lane 0 has declared their bytes on the stage barrier.  The
+  // stage may hold the previous phase's rows, read through the generic proxy
+  // by every warp before the CTA barrier that precedes this call.
+  __device__ __forceinline__ void issue_stage(int32_t ph, int lane, uint64_t* bar) const {
+    const int32_t* sb = ph ? sbd : sbu;
+    const int32_t span = ph ? span_d : span_u, elo = ph ? elo_d : elo_u;
+    const int32_t K = ph ? a.I : a.H;
+    const uint32_t RS = ph ? RSd : RSu;
+    const int32_t rows = span > 0 ? sb[span] : 0;
+    if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)rows * (uint32_t)K * 2u);
+    __syncwarp();
+    for (int32_t r = lane; r < rows; r += 32) {
+      int32_t j = 0;
+      while (j + 1 < span && sb[j + 1] <= r) ++j;
+      const int32_t pr = s_off[s_act[elo + j]] + (r - sb[j]);
+      const uint16_t* src;
+      if (ph == 0) {
+        const int32_t tok = a.ext ? __ldg(a.g_perm + pr) / a.k : s_tok[pr];
+        src = a.x + (size_t)tok * a.H;
+      } else {
+        src = a.Ap + (size_t)pr * a.I;
+      }
+      fence_proxy_async_smem();
+      bulk_g2s(stage + (size_t)r * RS, src, (uint32_t)K * 2u, bar);
+    }
+  }
 };
+
+// Work items of one CTA per phase: a work item is one 16-row tile of one
+// active expert, or two consecutive ones (p = 1) once some expert holds two
+// or more tokens (gated: always the gate and up tiles of the same rows).
+struct DecItems {
+  int32_t pu, pd, NPu, NPd, u_lo, n_up, d_lo, n_dn;
+};
+__device__ __forceinline__ DecItems dec_items(const DecodeArgs& a, int32_t n_act, int32_t cmax) {
+  DecItems it;
+  it.pd = cmax >= 2;
+  it.pu = it.pd || a.gated;
+  const int32_t NTu = (a.gated ? 2 * a.I : a.I) / 16, NTd = a.H / 16;
+  it.NPu = (NTu + it.pu) >> it.pu;
+  it.NPd = (NTd + it.pd) >> it.pd;
+  // n_act <= E <= 1024 and NP <= 256 (H, I <= 4096) keep U * G and D * G far below 2^32
+  const uint32_t G = gridDim.x, b = blockIdx.x;
+  const uint32_t U = (uint32_t)n_act * (uint32_t)it.NPu, D = (uint32_t)n_act * (uint32_t)it.NPd;
+  it.u_lo = (int32_t)(U * b / G);
+  it.d_lo = (int32_t)(D * b / G);
+  it.n_up = (int32_t)(U * (b + 1) / G) - it.u_lo;
+  it.n_dn = (int32_t)(D * (b + 1) / G) - it.d_lo;
+  return it;
+}
+
+// Warp 0, after the routing: decide whether this CTA stages its activation
+// rows (every expert holds at most 8 tokens, each phase's items span at most
+// kDecMaxSpan experts, and the larger phase's rows fit kDecStageMax bytes)
+// and write each phase's first stage row per expert.  misc[3] = staged,
+// misc[4] = stage bytes, misc[5..8] = first expert and span, up then down.
+__device__ __forceinline__ void decode_stage_plan(const DecodeArgs& a, int lane, const int32_t* s_counts,
+                                                  const int32_t* s_act, int32_t* misc, int32_t* s_sbase) {
+  __syncwarp();
+  const int32_t n_act = misc[1], cmax = misc[2];
+  if (cmax < 2 || cmax > kDecPassTok) {
+    // one token per expert: a chunk brings one activation row segment, and
+    // staging would save little against its planning on the critical path
+    if (lane == 0) misc[3] = 0;
+    return;
+  }
+  const DecItems it = dec_items(a, n_act, cmax);
+  bool ok = true;
+  uint32_t bytes = 0;
+#pragma unroll
+  for (int ph = 0; ph < 2; ++ph) {
+    const int32_t lo = ph ? it.d_lo : it.u_lo, n = ph ? it.n_dn : it.n_up, NP = ph ? it.NPd : it.NPu;
+    const int32_t elo = n > 0 ? lo / NP : 0;
+    const int32_t span = n > 0 ? (lo + n - 1) / NP - elo + 1 : 0;
+    ok = ok && span <= kDecMaxSpan;
+    const int32_t c = (ok && lane < span) ? s_counts[s_act[elo + lane]] : 0;
+    int32_t incl = c;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int32_t v = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += v;
+    }
+    const int32_t rows = __shfl_sync(0xffffffffu, incl, 31);
+    int32_t* sb = s_sbase + ph * (kDecMaxSpan + 1);
+    if (ok && lane < span) sb[lane + 1] = incl;
+    if (lane == 0) {
+      sb[0] = 0;
+      misc[5 + 2 * ph] = elo;
+      misc[6 + 2 * ph] = ok ? span : 0;
+    }
+    const uint32_t need = (uint32_t)rows * (uint32_t)(2 * (ph ? a.I : a.H) + 16);
+    bytes = need > bytes ? need : bytes;
+  }
+  bytes = (bytes + 127u) & ~127u;
+  ok = ok && bytes <= (uint32_t)kDecStageMax;
+  if (lane == 0) {
+    misc[3] = ok;
+    misc[4] = ok ? (int32_t)bytes : 0;
+  }
+}
 
 // One k-tile (16 rows x 64 k) of one row tile against this lane's activation
 // fragments x0 (k 16t .. 16t+7) and x1 (k 16t+8 .. 16t+15) of token column g.
@@ -609,6 +725,151 @@ __device__ __forceinline__ void combine_one(const DecodeArgs& a, const int32_t* 
   a.dst_out[o] = f2bf_rn(acc);
 }
 
+// One warp from its ring fill through the grid barrier to the drain of its
+// copies.  STAGED: the activation fragments come from the CTA-wide stage,
+// otherwise from each chunk's own activation copies (compiled separately so
+// that neither loop carries the other's addressing).
+template <bool STAGED>
+__device__ __forceinline__ void decode_stream(const DecodeArgs& a, const DecodeCtx& cx, uint8_t* ring,
+                                              uint32_t slot_bytes, int32_t P, uint64_t* wbar, Cur* wdesc,
+                                              uint64_t* stage_bar, const uint32_t* lut, float4* partial,
+                                              int32_t* pcount, const int32_t* s_inv, int32_t n_act, int tid,
+                                              int nthreads) {
+  const int lane = tid & 31, warp = tid >> 5;
+  const uint32_t wbytes = cx.wbytes;
+  const uint64_t pol = policy_evict_first();
+
+  // Chunk q of this warp's sequence lives in slot q % P.  Its weights are
+  // requested P chunks ahead; its activations too, except down chunks issued
+  // before the grid barrier, whose activations follow right after it.
+  Cur ci;
+  cx.template enter_phase<STAGED>(ci, 0);
+  int32_t issued = 0, acts_issued = 0;
+  bool crossed = false, dead = false;
+  auto issue = [&](int32_t s) {
+    uint8_t* sp = ring + (size_t)s * slot_bytes;
+    if (lane == 0) {
+      wdesc[s] = ci;
+      cx.template issue_weights<STAGED>(ci, sp, &wbar[s], pol);
+    }
+    if (ci.ph == 0 || crossed) {
+      cx.template issue_acts<STAGED>(ci, lane, sp, &wbar[s]);
+      ++acts_issued;
+    }
+    cx.template advance<STAGED>(ci);
+    ++issued;
+  };
+  // The up phase's staged activation rows go first, then the rings fill in
+  // rounds -- every warp's first chunk, then every warp's second, ... -- so
+  // that the copies needed first lead the SM's copy queue.
+  int32_t stage_issued = 0, stage_seen = 0;
+  if (STAGED && warp == 0) {
+    cx.issue_stage(0, lane, stage_bar);
+    stage_issued = 1;
+  }
+  for (int32_t s = 0; s < P; ++s) {
+    if (ci.ph < 2) issue(s);
+    all_warps_sync(nthreads);
+  }
+
+  int32_t consumed = 0, slot = 0;
+  uint32_t phase = 0;
+  float accA[4] = {0.f, 0.f, 0.f, 0.f}, accA2[4] = {0.f, 0.f, 0.f, 0.f};
+  float accB[4] = {0.f, 0.f, 0.f, 0.f}, accB2[4] = {0.f, 0.f, 0.f, 0.f};
+  while (consumed < issued) {
+    const Cur cur = wdesc[slot];
+    if (cur.ph == 1 && !crossed) {
+      // every up tile of every CTA is stored before any down tile reads Ap
+      decode_grid_barrier(a, tid, nthreads);
+      crossed = true;
+      if (STAGED && warp == 0) {
+        cx.issue_stage(1, lane, stage_bar);
+        stage_issued = 2;
+      }
+      for (int32_t q = acts_issued; q < issued; ++q) {
+        const int32_t s = q % P;
+        cx.template issue_acts<STAGED>(wdesc[s], lane, ring + (size_t)s * slot_bytes, &wbar[s]);
+      }
+      acts_issued = issued;
+    }
+    bool ok = mbar_wait_sleep(&wbar[slot], phase, a.err);
+    if (STAGED && ok && stage_seen <= cur.ph) {
+      // the stage's phase cur.ph is the CTA barrier's phase of the same number
+      ok = mbar_wait_sleep(stage_bar, (uint32_t)cur.ph, a.err);
+      stage_seen = cur.ph + 1;
+    }
+    if (__any_sync(0xffffffffu, !ok)) {
+      dead = true;
+      break;
+    }
+    if (consumed == 0 && lane == 0) {
+      // once the first chunk has landed, ask L2 for the chunks past the ring
+      Cur cp = ci;
+      for (int q = 0; q < kDecL2Ahead && cp.ph < 2; ++q) {
+        const uint8_t* src = cx.chunk_src(cp);
+        prefetch_l2_bulk(src, (uint32_t)cx.kts(cp) * kTileBytes);
+        if (cx.two(cp))
+          prefetch_l2_bulk(src + (size_t)(cp.ph ? cx.KTd : cx.KTu) * kTileBytes, (uint32_t)cx.kts(cp) * kTileBytes);
+        cx.template advance<STAGED>(cp);
+      }
+    }
+    const uint8_t* sp = ring + (size_t)slot * slot_bytes;
+    const int32_t nt = min(kDecPassTok, cur.cnt - cur.tok0);
+    const int32_t col = min(lane >> 2, nt - 1);
+    const uint8_t* act =
+        STAGED ? cx.stage + (size_t)(cur.srow + col) * (cur.ph ? cx.RSd : cx.RSu) + cur.kt * 128 + (lane & 3) * 32
+               : sp + wbytes + col * kDecActRow + (lane & 3) * 32;
+    chunk_mma(sp, act, cx.kts(cur), cx.two(cur), lane, lut, accA, accA2, accB, accB2);
+    ++consumed;
+    __syncwarp();
+    if (ci.ph < 2) {
+      if (lane == 0) fence_proxy_async_smem();
+      issue(slot);
+      __syncwarp();
+    }
+    if (++slot == P) {
+      slot = 0;
+      phase ^= 1u;
+    }
+    if (cur.kt + kDecCK >= cur.kt_end) {
+      float v[8];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        v[q] = accA[q] + accA2[q];
+        v[4 + q] = accB[q] + accB2[q];
+        accA[q] = accA2[q] = accB[q] = accB2[q] = 0.f;
+      }
+      decode_epilogue(cx, cur, v, lane, partial, pcount, s_inv, n_act);
+    }
+  }
+  if (!crossed) {
+    decode_grid_barrier(a, tid, nthreads);
+    if (STAGED && warp == 0) {
+      cx.issue_stage(1, lane, stage_bar);
+      stage_issued = 2;
+    }
+  }
+  if (stage_issued > 0) {
+    // (warp 0) the stage copies it issued land before the CTA can exit; the
+    // last phase issued completes after the earlier one
+    mbar_wait_sleep(stage_bar, (uint32_t)(stage_issued - 1), a.err);
+  }
+  if (dead) {
+    // let this warp's copies still in flight land before the CTA exits; the
+    // chunks whose activations were never requested get them now (in-bounds
+    // reads of whatever the rows hold) so that their barriers can complete
+    for (int32_t q = acts_issued; q < issued; ++q) {
+      const int32_t s = q % P;
+      cx.template issue_acts<STAGED>(wdesc[s], lane, ring + (size_t)s * slot_bytes, &wbar[s]);
+    }
+    for (int32_t q = consumed; q < issued; ++q) mbar_wait_sleep(&wbar[q % P], (uint32_t)((q / P) & 1), a.err);
+  }
+}
+
+// CAN_STAGE = false compiles the per-chunk activation path alone: a batch of
+// one token has one token per expert, where staging never applies, and that
+// loop then keeps the registers and code layout it has on its own.
+template <bool CAN_STAGE>
 __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) decode_kernel(const __grid_constant__ DecodeArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const DecLayout& L = a.L;
@@ -621,6 +882,8 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) decode_kernel(const __gr
   int32_t* s_act = reinterpret_cast<int32_t*>(smem + L.act);
   int32_t* misc = reinterpret_cast<int32_t*>(smem + L.misc);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
+  uint64_t* stage_bar = bars + kDecMaxSlots * kDecMaxWarps;
+  int32_t* s_sbase = reinterpret_cast<int32_t*>(smem + L.sbase);
   float4* partial = reinterpret_cast<float4*>(smem + L.partial);
   int32_t* pcount = reinterpret_cast<int32_t*>(smem + L.pcount);
   Cur* descs = reinterpret_cast<Cur*>(smem + L.desc);
@@ -658,6 +921,7 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) decode_kernel(const __gr
   if (lane == 0) {
     // one arrival: lane 0's expect_tx covering the weight and activation copies
     for (int q = 0; q < kDecMaxSlots; ++q) mbar_init(&bars[warp * kDecMaxSlots + q], 1);
+    if (warp == 0) mbar_init(stage_bar, 1);  // one arrival per phase: warp 0 lane 0's expect_tx
     fence_mbar_init();
   }
   __syncthreads();
@@ -674,6 +938,7 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) decode_kernel(const __gr
     __syncthreads();
     if (warp == 0) decode_route(a, lane, s_ids, s_tok, s_inv, s_counts, s_off, s_act, misc);
   }
+  if (CAN_STAGE && warp == 0) decode_stage_plan(a, lane, s_counts, s_act, misc, s_sbase);
   __syncthreads();
 
   const int32_t n_act = misc[1], cmax = misc[2];
@@ -683,11 +948,22 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) decode_kernel(const __gr
   // activation fragments are then loaded once for both); single tiles keep
   // the chunks small where the layer is all latency.  A gated up projection
   // always takes its gate and up tiles together.
-  const int32_t pd = cmax >= 2, pu = pd || a.gated;
+  const DecItems it = dec_items(a, n_act, cmax);
+  const int32_t pd = it.pd, pu = it.pu;
   const uint32_t wbytes = pu ? kDecSlotBytes : kDecCK * kTileBytes;
-  const uint32_t slot_bytes = wbytes + nt_cap * kDecActRow;
-  const uint32_t ring_bytes = L.total - L.ring;
-  const int32_t Weff = max(1, min(W, (int32_t)(ring_bytes / (2u * slot_bytes))));
+  // Staged rows replace the activation part of every slot; stage only if
+  // that leaves at least as many streaming warps as per-chunk copies would.
+  const uint32_t region = L.total - L.ring;
+  const uint32_t copy_slot = wbytes + nt_cap * kDecActRow;
+  const int32_t W_copy = max(1, min(W, (int32_t)(region / (2u * copy_slot))));
+  const bool plan_ok = CAN_STAGE && misc[3] != 0;
+  const uint32_t planned = plan_ok ? (uint32_t)misc[4] : region;
+  const int32_t W_stage = planned < region ? max(1, min(W, (int32_t)((region - planned) / (2u * wbytes)))) : 0;
+  const bool staged = plan_ok && W_stage >= W_copy;
+  const uint32_t stage_bytes = staged ? planned : 0u;
+  const uint32_t slot_bytes = staged ? wbytes : copy_slot;
+  const uint32_t ring_bytes = region - stage_bytes;
+  const int32_t Weff = staged ? W_stage : W_copy;
   const int32_t P = min(kDecMaxSlots, (int32_t)(ring_bytes / ((uint32_t)Weff * slot_bytes)));
 
   DecodeCtx cx(a);
@@ -695,14 +971,19 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) decode_kernel(const __gr
   cx.warp = warp; cx.W = Weff;
   cx.KTu = a.H / 64; cx.KTd = a.I / 64; cx.NTu = (a.gated ? 2 * a.I : a.I) / 16; cx.NTd = a.H / 16;
   cx.pu = pu; cx.pd = pd; cx.wbytes = wbytes;
-  cx.NPu = (cx.NTu + pu) >> pu; cx.NPd = (cx.NTd + pd) >> pd;
+  cx.NPu = it.NPu; cx.NPd = it.NPd;
+  cx.staged = staged;
+  cx.stage = smem + L.total - stage_bytes;
+  cx.RSu = 2u * (uint32_t)a.H + 16u;
+  cx.RSd = 2u * (uint32_t)a.I + 16u;
+  cx.sbu = s_sbase;
+  cx.sbd = s_sbase + (kDecMaxSpan + 1);
+  cx.elo_u = misc[5]; cx.span_u = misc[6]; cx.elo_d = misc[7]; cx.span_d = misc[8];
   {
-    const int64_t G = gridDim.x, b = blockIdx.x;
-    const int64_t U = (int64_t)n_act * cx.NPu, D = (int64_t)n_act * cx.NPd;
-    cx.u_lo = (int32_t)(U * b / G);
-    cx.d_lo = (int32_t)(D * b / G);
-    cx.n_up = (int32_t)(U * (b + 1) / G) - cx.u_lo;
-    cx.n_dn = (int32_t)(D * (b + 1) / G) - cx.d_lo;
+    cx.u_lo = it.u_lo;
+    cx.d_lo = it.d_lo;
+    cx.n_up = it.n_up;
+    cx.n_dn = it.n_dn;
     cx.split = cmax <= kDecPassTok;
     const int64_t TTu = (int64_t)cx.n_up * cx.KTu, TTd = (int64_t)cx.n_dn * cx.KTd;
     cx.Wu = (int32_t)(TTu < Weff ? TTu : Weff);
@@ -715,104 +996,12 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) decode_kernel(const __gr
   uint8_t* ring = smem + L.ring + (size_t)min(warp, Weff - 1) * P * slot_bytes;
   uint64_t* wbar = bars + warp * kDecMaxSlots;
   Cur* wdesc = descs + warp * kDecMaxSlots;
-  const uint64_t pol = policy_evict_first();
-
-  // Chunk q of this warp's sequence lives in slot q % P.  Its weights are
-  // requested P chunks ahead; its activations too, except down chunks issued
-  // before the grid barrier, whose activations follow right after it.
-  Cur ci;
-  cx.enter_phase(ci, 0);
-  int32_t issued = 0, acts_issued = 0;
-  bool crossed = false, dead = false;
-  auto issue = [&](int32_t s) {
-    uint8_t* sp = ring + (size_t)s * slot_bytes;
-    if (lane == 0) {
-      wdesc[s] = ci;
-      cx.issue_weights(ci, sp, &wbar[s], pol);
-    }
-    if (ci.ph == 0 || crossed) {
-      cx.issue_acts(ci, lane, sp, &wbar[s]);
-      ++acts_issued;
-    }
-    cx.advance(ci);
-    ++issued;
-  };
-  // Fill the rings in rounds -- every warp's first chunk, then every warp's
-  // second, ... -- so that the copies needed first lead the SM's copy queue.
-  for (int32_t s = 0; s < P; ++s) {
-    if (ci.ph < 2) issue(s);
-    all_warps_sync(nthreads);
-  }
-
-  int32_t consumed = 0, slot = 0;
-  uint32_t phase = 0;
-  float accA[4] = {0.f, 0.f, 0.f, 0.f}, accA2[4] = {0.f, 0.f, 0.f, 0.f};
-  float accB[4] = {0.f, 0.f, 0.f, 0.f}, accB2[4] = {0.f, 0.f, 0.f, 0.f};
-  while (consumed < issued) {
-    const Cur cur = wdesc[slot];
-    if (cur.ph == 1 && !crossed) {
-      // every up tile of every CTA is stored before any down tile reads Ap
-      decode_grid_barrier(a, tid, nthreads);
-      crossed = true;
-      for (int32_t q = acts_issued; q < issued; ++q) {
-        const int32_t s = q % P;
-        cx.issue_acts(wdesc[s], lane, ring + (size_t)s * slot_bytes, &wbar[s]);
-      }
-      acts_issued = issued;
-    }
-    const bool ok = mbar_wait_sleep(&wbar[slot], phase, a.err);
-    if (__any_sync(0xffffffffu, !ok)) {
-      dead = true;
-      break;
-    }
-    if (consumed == 0 && lane == 0) {
-      // once the first chunk has landed, ask L2 for the chunks past the ring
-      Cur cp = ci;
-      for (int q = 0; q < kDecL2Ahead && cp.ph < 2; ++q) {
-        const uint8_t* src = cx.chunk_src(cp);
-        prefetch_l2_bulk(src, (uint32_t)cx.kts(cp) * kTileBytes);
-        if (cx.two(cp))
-          prefetch_l2_bulk(src + (size_t)(cp.ph ? cx.KTd : cx.KTu) * kTileBytes, (uint32_t)cx.kts(cp) * kTileBytes);
-        cx.advance(cp);
-      }
-    }
-    const uint8_t* sp = ring + (size_t)slot * slot_bytes;
-    const int32_t nt = min(kDecPassTok, cur.cnt - cur.tok0);
-    const uint8_t* act = sp + wbytes + min(lane >> 2, nt - 1) * kDecActRow + (lane & 3) * 32;
-    chunk_mma(sp, act, cx.kts(cur), cx.two(cur), lane, lut, accA, accA2, accB, accB2);
-    ++consumed;
-    __syncwarp();
-    if (ci.ph < 2) {
-      if (lane == 0) fence_proxy_async_smem();
-      issue(slot);
-      __syncwarp();
-    }
-    if (++slot == P) {
-      slot = 0;
-      phase ^= 1u;
-    }
-    if (cur.kt + kDecCK >= cur.kt_end) {
-      float v[8];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        v[q] = accA[q] + accA2[q];
-        v[4 + q] = accB[q] + accB2[q];
-        accA[q] = accA2[q] = accB[q] = accB2[q] = 0.f;
-      }
-      decode_epilogue(cx, cur, v, lane, partial, pcount, s_inv, n_act);
-    }
-  }
-  if (!crossed) decode_grid_barrier(a, tid, nthreads);
-  if (dead) {
-    // let this warp's copies still in flight land before the CTA exits; the
-    // chunks whose activations were never requested get them now (in-bounds
-    // reads of whatever the rows hold) so that their barriers can complete
-    for (int32_t q = acts_issued; q < issued; ++q) {
-      const int32_t s = q % P;
-      cx.issue_acts(wdesc[s], lane, ring + (size_t)s * slot_bytes, &wbar[s]);
-    }
-    for (int32_t q = consumed; q < issued; ++q) mbar_wait_sleep(&wbar[q % P], (uint32_t)((q / P) & 1), a.err);
-  }
+  if (CAN_STAGE && staged)
+    decode_stream<true>(a, cx, ring, slot_bytes, P, wbar, wdesc, stage_bar, lut, partial, pcount, s_inv, n_act,
+                        tid, nthreads);
+  else
+    decode_stream<false>(a, cx, ring, slot_bytes, P, wbar, wdesc, stage_bar, lut, partial, pcount, s_inv, n_act,
+                         tid, nthreads);
   if (!a.ext && a.n > kDecLateCombine) {
     // every down row of every CTA is stored: combine, one element per thread
     decode_grid_barrier(a, tid, nthreads);
@@ -825,8 +1014,10 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) decode_kernel(const __gr
 DecLayout decode_layout(int32_t E, int32_t R) { return dec_layout(E, R, 227 * 1024 - 1024); }
 
 cudaError_t launch_decode(const DecodeArgs& args, int num_sms, cudaStream_t s) {
-  static std::atomic<bool> attr_set[kMaxDevices];
-  cudaError_t e = raise_smem_limit(decode_kernel, 227 * 1024, attr_set);
+  static std::atomic<bool> attr_set[2][kMaxDevices];
+  const bool can_stage = args.n > 1 || args.ext;
+  auto kernel = can_stage ? decode_kernel<true> : decode_kernel<false>;
+  cudaError_t e = raise_smem_limit(kernel, 227 * 1024, attr_set[can_stage ? 1 : 0]);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)num_sms);
@@ -838,7 +1029,7 @@ cudaError_t launch_decode(const DecodeArgs& args, int num_sms, cudaStream_t s) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_kernel, args);
+  return cudaLaunchKernelEx(&cfg, kernel, args);
 }
 
 }  // namespace moe

@@ -125,12 +125,14 @@ constexpr int kDecPassTok = 8;         // tokens per pass over a tile (one n8 MM
 constexpr int kDecL2Ahead = 8;         // chunks past the ring requested into L2 at start
 constexpr long long kDecEarlyL2Bytes = 48ll << 20;  // picked experts' up weights prefetched during routing, at most
 constexpr int kDecLateCombine = 8;     // larger batches combine after a second grid barrier
+constexpr int kDecMaxSpan = 16;        // experts whose activation rows one CTA stages per phase, at most
+constexpr int kDecStageMax = 96 * 1024;  // bytes of staged activation rows per CTA, at most
 constexpr int kDecMaxPairs = 1024;     // batches with at most this many pairs
 constexpr int kDecMaxTokens = 64;      // and tokens run as one launch
 
 // Shared-memory plan of the decode kernel (byte offsets; the host computes it).
 struct DecLayout {
-  uint32_t scale_lut, ids, perm, inv, counts, offsets, act, misc, bars, partial, pcount, desc, ring, total;
+  uint32_t scale_lut, ids, perm, inv, counts, offsets, act, misc, bars, partial, pcount, desc, sbase, ring, total;
   uint32_t warps;
 };
 
@@ -151,10 +153,11 @@ inline DecLayout dec_layout(int32_t E, int32_t R, uint32_t budget) {
   L.offsets = take(4 * ((uint32_t)E + 1), 16);
   L.act = take(4 * (uint32_t)E, 16);
   L.misc = take(64, 16);
-  L.bars = take(8 * kDecMaxSlots * kDecMaxWarps, 16);
+  L.bars = take(8 * (kDecMaxSlots * kDecMaxWarps + 1), 16);  // ring slots, then the stage barrier
   L.partial = take(2 * kDecMaxWarps * 32 * 32, 128);  // (warp, first/last segment) x lanes x 2 float4
   L.pcount = take(kDecMaxWarps * 4, 16);
   L.desc = take(kDecMaxWarps * kDecMaxSlots * 48, 16);  // per-slot chunk descriptors
+  L.sbase = take(4 * 2 * (kDecMaxSpan + 1), 16);        // per phase: first stage row of each staged expert
   const uint32_t ring_at = (o + 127) / 128 * 128;
   uint32_t warps = budget > ring_at ? (budget - ring_at) / (2 * kDecSlotBytes) : 0;
   if (warps > (uint32_t)kDecMaxWarps) warps = kDecMaxWarps;
