@@ -79,6 +79,8 @@ struct moe_nvfp4 {
   float* gate_g = nullptr;
   // the same weights in fragment-tile order for the single-launch small-batch path
   uint8_t *up_tiles = nullptr, *dn_tiles = nullptr;
+  // and with whole code bytes in fragment order for its f16 path (batches of several tokens)
+  uint8_t *up_tiles16 = nullptr, *dn_tiles16 = nullptr;
   // and in packed 128-row blocks for the grouped GEMM
   uint8_t *up_blocks = nullptr, *dn_blocks = nullptr;
   int32_t *col_done = nullptr, *grid_bar = nullptr;
@@ -122,6 +124,7 @@ void free_handle(moe_nvfp4* h) {
                   h->counts,   h->offsets,   h->perm_pair, h->inv,      h->err,       h->Xp,
                   h->Ap,       h->Yp,        h->x_stage,   h->dst_stage, h->ids_stage, h->w_stage,
                   h->up_tiles, h->dn_tiles,  h->col_done,  h->grid_bar,  h->up_blocks, h->dn_blocks,
+                  h->up_tiles16, h->dn_tiles16,
                   h->gate_codes, h->gate_scales, h->gate_g, h->blk_hist, h->dense_ids, h->dense_w};
   for (void* p : ptrs)
     if (p) cudaFree(p);
@@ -285,6 +288,8 @@ moe_status moe_nvfp4_create(const moe_nvfp4_config* config, const moe_nvfp4_weig
   }
   TRY(cudaMalloc(&h->up_tiles, (mat_codes + mat_scales) * (gated ? 2 : 1)));
   TRY(cudaMalloc(&h->dn_tiles, mat_codes + mat_scales));
+  TRY(cudaMalloc(&h->up_tiles16, (mat_codes + mat_scales) * (gated ? 2 : 1)));
+  TRY(cudaMalloc(&h->dn_tiles16, mat_codes + mat_scales));
   TRY(cudaMalloc(&h->up_blocks, gemm_blocks_bytes((int32_t)E, (int32_t)up_rows, (int32_t)H)));
   TRY(cudaMalloc(&h->dn_blocks, gemm_blocks_bytes((int32_t)E, (int32_t)H, (int32_t)I)));
   TRY(cudaMalloc(&h->col_done, (H / 16) * sizeof(int32_t)));
@@ -329,12 +334,15 @@ moe_status moe_nvfp4_create(const moe_nvfp4_config* config, const moe_nvfp4_weig
     TRY(cudaMemcpy2DAsync(gu_scales + sblk, 2 * sblk, h->up_scales, sblk, sblk, groups, cudaMemcpyDeviceToDevice,
                           s));
     TRY(launch_repack_frag(gu_codes, gu_scales, (int32_t)E, (int32_t)up_rows, (int32_t)H, h->up_tiles, s));
+    TRY(launch_repack_frag16(gu_codes, gu_scales, (int32_t)E, (int32_t)up_rows, (int32_t)H, h->up_tiles16, s));
     TRY(launch_repack_gemm(gu_codes, gu_scales, (int32_t)E, (int32_t)up_rows, (int32_t)H, h->up_blocks, s));
   } else {
     TRY(launch_repack_frag(h->up_codes, h->up_scales, (int32_t)E, (int32_t)I, (int32_t)H, h->up_tiles, s));
+    TRY(launch_repack_frag16(h->up_codes, h->up_scales, (int32_t)E, (int32_t)I, (int32_t)H, h->up_tiles16, s));
     TRY(launch_repack_gemm(h->up_codes, h->up_scales, (int32_t)E, (int32_t)I, (int32_t)H, h->up_blocks, s));
   }
   TRY(launch_repack_frag(h->dn_codes, h->dn_scales, (int32_t)E, (int32_t)H, (int32_t)I, h->dn_tiles, s));
+  TRY(launch_repack_frag16(h->dn_codes, h->dn_scales, (int32_t)E, (int32_t)H, (int32_t)I, h->dn_tiles16, s));
   TRY(launch_repack_gemm(h->dn_codes, h->dn_scales, (int32_t)E, (int32_t)H, (int32_t)I, h->dn_blocks, s));
   TRY(make_tmap_act_rows(&h->tm_xp, h->Xp, Rr, H, kGemmTileRows));
   TRY(make_tmap_act_rows(&h->tm_ap, h->Ap, Rr, I, kGemmTileRows));
@@ -377,6 +385,8 @@ static moe_status forward_impl(moe_nvfp4* h, const uint16_t* x, const int32_t* i
   DecodeArgs d{};
   d.up_tiles = h->up_tiles;
   d.dn_tiles = h->dn_tiles;
+  d.up_tiles16 = h->up_tiles16;
+  d.dn_tiles16 = h->dn_tiles16;
   d.up_g = h->up_g;
   d.dn_g = h->dn_g;
   d.gate_g = h->gate_g;

@@ -118,7 +118,84 @@ cudaError_t launch_repack_frag(const uint8_t* codes, const uint8_t* scales, int3
   return cudaGetLastError();
 }
 
+// Byte-order fragment tiles for the f16 path: the same [G][N/16][K/64] tiles
+// of 576 bytes and the same scale bytes, but lane (g, t)'s 16 code bytes are
+// whole NVFP4 bytes (two consecutive k, the lower k in the low nibble), in the
+// order the f16 MMA takes them.  Word j serves MMA j of the k-tile, which sums
+// k = 16t + 4j .. 16t + 4j + 3 of this lane (the lane's 16 consecutive k are
+// still one scale block per row): bytes [row g, k 16t+4j..+1], [row g+8, the
+// same], [row g, k 16t+4j+2..+3], [row g+8, the same] = A registers a0..a3.
+__global__ void repack_frag16_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
+                                     int32_t G, int32_t N, int32_t K, uint8_t* __restrict__ out) {
+  const int32_t KT = K / 64, NT = N / 16;
+  const long long tiles = (long long)G * NT * KT;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < tiles * 32;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long tile = i >> 5;
+    const int lane = (int)(i & 31);
+    const int kt = (int)(tile % KT);
+    const long long rest = tile / KT;
+    const int rt = (int)(rest % NT);
+    const long long grp = rest / NT;
+    const int g = lane >> 2, t = lane & 3;
+    const uint8_t* row0 = codes + (grp * N + rt * 16 + g) * (long long)(K / 2) + kt * 32 + 8 * t;
+    const uint8_t* row8 = row0 + 8LL * (K / 2);
+    uint32_t* dst = reinterpret_cast<uint32_t*>(out + tile * kTileBytes + 16 * lane);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      dst[j] = (uint32_t)row0[2 * j] | ((uint32_t)row8[2 * j] << 8) | ((uint32_t)row0[2 * j + 1] << 16) |
+               ((uint32_t)row8[2 * j + 1] << 24);
+    if (lane < 16) {
+      const long long row = grp * N + rt * 16 + lane;
+      uint8_t* sd = out + tile * kTileBytes + 512 + 4 * lane;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) sd[j] = scales[row * (K / 16) + kt * 4 + j];
+    }
+  }
+}
+
+cudaError_t launch_repack_frag16(const uint8_t* codes, const uint8_t* scales, int32_t G, int32_t N, int32_t K,
+                                 uint8_t* out, cudaStream_t s) {
+  const long long work = (long long)G * (N / 16) * (K / 64) * 32;
+  long long blocks = (work + 255) / 256;
+  if (blocks > 65535LL * 8) blocks = 65535LL * 8;
+  if (blocks < 1) blocks = 1;
+  repack_frag16_kernel<<<(unsigned)blocks, 256, 0, s>>>(codes, scales, G, N, K, out);
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ helpers
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// The four NVFP4 bytes of w as f16 pairs (hardware conversion: the low
+// nibble becomes the low half), exact.
+__device__ __forceinline__ void e2m1x8_to_f16(uint32_t w, uint32_t& p0, uint32_t& p1, uint32_t& p2, uint32_t& p3) {
+  asm("{.reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;}"
+      : "=r"(p0), "=r"(p1), "=r"(p2), "=r"(p3)
+      : "r"(w));
+}
+__device__ __forceinline__ uint32_t mul_f16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// f16 pair (both halves) of an e4m3 byte's value, exact: |v| <= 448 and the
+// smallest subnormal 2^-9 are normal f16 numbers with at most 4 significant bits.
+__device__ __forceinline__ uint32_t scale_f16x2(uint32_t b) {
+  const uint32_t e = (b >> 3) & 15u, m = b & 7u;
+  float v = e ? (float)(8u + m) * __uint_as_float((e - 10u + 127u) << 23) : (float)m * 0x1p-9f;
+  if (b & 0x80u) v = -v;
+  const uint32_t h = (uint32_t)__half_as_ushort(__float2half_rn(v));
+  return h | (h << 16);
+}
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                                uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -272,9 +349,11 @@ struct DecodeCtx {
     }
     enter_phase<S>(c, c.ph + 1);
   }
+  // Staged chunks stream the byte-order tiles of the f16 path.
+  template <bool S>
   __device__ __forceinline__ const uint8_t* chunk_src(const Cur& c) const {
     const int32_t KT = c.ph ? KTd : KTu, NT = c.ph ? NTd : NTu;
-    const uint8_t* base = c.ph ? a.dn_tiles : a.up_tiles;
+    const uint8_t* base = S ? (c.ph ? a.dn_tiles16 : a.up_tiles16) : (c.ph ? a.dn_tiles : a.up_tiles);
     return base + ((size_t)((size_t)c.e * NT + c.rt) * KT + c.kt) * kTileBytes;
   }
   __device__ __forceinline__ int32_t kts(const Cur& c) const { return min(kDecCK, c.kt_end - c.kt); }
@@ -291,7 +370,7 @@ struct DecodeCtx {
     const uint32_t nt = (uint32_t)min(kDecPassTok, c.cnt - c.tok0);
     const bool pair = two(c);
     mbar_arrive_expect_tx(bar, n_kt * ((pair ? 2u : 1u) * kTileBytes + (S ? 0u : nt * 128u)));
-    const uint8_t* src = chunk_src(c);
+    const uint8_t* src = chunk_src<S>(c);
     bulk_g2s_hint(slot, src, n_kt * kTileBytes, bar, pol);
     if (pair)
       bulk_g2s_hint(slot + kDecCK * kTileBytes, src + (size_t)(c.ph ? KTd : KTu) * kTileBytes, n_kt * kTileBytes,
@@ -458,6 +537,40 @@ __device__ __forceinline__ void chunk_mma(const uint8_t* wts, const uint8_t* act
   }
 }
 
+// f16 forms of the two above, on byte-order tiles (repack_frag16_kernel) and
+// f16 activation rows: word j of the lane's codes is MMA j's A fragment, each
+// pair multiplied by the row's scale (f16, exact: codes have 2 and scales at
+// most 4 significant bits, the product lies in [2^-10, 2688]).
+__device__ __forceinline__ void tile_mma16(const uint8_t* tile, const uint4& x0, const uint4& x1, int lane,
+                                           const uint32_t* lut16, float (&acc)[4], float (&acc2)[4]) {
+  const int g = lane >> 2, t = lane & 3;
+  const uint4 c = *reinterpret_cast<const uint4*>(tile + 16 * lane);
+  const uint32_t s0 = lut16[tile[512 + 4 * g + t]];
+  const uint32_t s1 = lut16[tile[512 + 4 * (g + 8) + t]];
+  uint32_t p0, p1, p2, p3;
+  e2m1x8_to_f16(c.x, p0, p1, p2, p3);
+  mma_f16_16816(acc, mul_f16x2(p0, s0), mul_f16x2(p1, s1), mul_f16x2(p2, s0), mul_f16x2(p3, s1), x0.x, x0.y);
+  e2m1x8_to_f16(c.y, p0, p1, p2, p3);
+  mma_f16_16816(acc2, mul_f16x2(p0, s0), mul_f16x2(p1, s1), mul_f16x2(p2, s0), mul_f16x2(p3, s1), x0.z, x0.w);
+  e2m1x8_to_f16(c.z, p0, p1, p2, p3);
+  mma_f16_16816(acc, mul_f16x2(p0, s0), mul_f16x2(p1, s1), mul_f16x2(p2, s0), mul_f16x2(p3, s1), x1.x, x1.y);
+  e2m1x8_to_f16(c.w, p0, p1, p2, p3);
+  mma_f16_16816(acc2, mul_f16x2(p0, s0), mul_f16x2(p1, s1), mul_f16x2(p2, s0), mul_f16x2(p3, s1), x1.z, x1.w);
+}
+__device__ __forceinline__ void chunk_mma16(const uint8_t* wts, const uint8_t* act, int kts, bool pair, int lane,
+                                            const uint32_t* lut16, float (&accA)[4], float (&accA2)[4],
+                                            float (&accB)[4], float (&accB2)[4]) {
+#pragma unroll
+  for (int kt = 0; kt < kDecCK; ++kt) {
+    if (kt < kts) {
+      const uint4 x0 = *reinterpret_cast<const uint4*>(act + kt * 128);
+      const uint4 x1 = *reinterpret_cast<const uint4*>(act + kt * 128 + 16);
+      tile_mma16(wts + kt * kTileBytes, x0, x1, lane, lut16, accA, accA2);
+      if (pair) tile_mma16(wts + (kDecCK + kt) * kTileBytes, x0, x1, lane, lut16, accB, accB2);
+    }
+  }
+}
+
 // ------------------------------------------------------------ kernel
 // Routing of all pairs by warp 0, into shared memory (every CTA computes the
 // same result; CTA 0 also writes it out).  Stable: pairs of one expert keep
@@ -600,7 +713,7 @@ __device__ __forceinline__ void decode_grid_barrier(const DecodeArgs& a, int tid
 // combine after a second grid barrier).
 __device__ __forceinline__ void decode_epilogue(const DecodeCtx& cx, const Cur& cur, float (&v)[8], int lane,
                                                 float4* partial, int32_t* pcount, const int32_t* s_inv,
-                                                int32_t n_act) {
+                                                int32_t n_act, const float* rowscale) {
   const DecodeArgs& a = cx.a;
   const int32_t up = cur.ph == 0;
   const bool pair = cx.two(cur);
@@ -641,11 +754,18 @@ __device__ __forceinline__ void decode_epilogue(const DecodeCtx& cx, const Cur& 
     }
   }
   const int g = lane >> 2, t = lane & 3;
-  const float alpha = (up ? a.up_g : a.dn_g)[cur.e] * 256.0f;
   const int32_t nt = min(kDecPassTok, cur.cnt - cur.tok0);
+  // bf16 path: the weights were taken times 2^-8 (alpha carries 2^8); f16
+  // path (rowscale): exact weights, each token column's rows times 2^-s
+  const float wfix = rowscale ? 1.0f : 256.0f;
+  if (rowscale) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) v[q] *= rowscale[cur.srow + min(2 * t + (q & 1), nt - 1)];
+  }
+  const float alpha = (up ? a.up_g : a.dn_g)[cur.e] * wfix;
   if (up && a.gated) {
     // the pair is (gate tile, up tile) of the same 16 intermediate rows
-    const float ag = a.gate_g[cur.e] * 256.0f;
+    const float ag = a.gate_g[cur.e] * wfix;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int32_t col = 2 * t + (q & 1);
@@ -725,6 +845,57 @@ __device__ __forceinline__ void combine_one(const DecodeArgs& a, const int32_t* 
   a.dst_out[o] = f2bf_rn(acc);
 }
 
+// bf16 pair w times `down` (a power of two) as an f16 pair.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, float down) {
+  const __half2 h = __floats2half2_rn(__uint_as_float(w << 16) * down, __uint_as_float(w & 0xFFFF0000u) * down);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t w, uint32_t m) {
+  return max(m, max(w & 0x7FFFu, (w >> 16) & 0x7FFFu));
+}
+
+// All threads of the CTA: wait for phase ph's staged bf16 rows, then rewrite
+// each in place as f16 values times 2^-s, with s per row putting the row's
+// largest magnitude in [2^14, 2^15) (s clamped to [-126, 126]), and keep 2^s
+// for the epilogue.  A bf16 value is then an f16 number exactly unless its
+// scaled magnitude is below 2^-14 -- 2^28 under the row's largest -- where the
+// f16 subnormal spacing 2^-24 rounds it.  The CTA barrier at the end orders
+// the rewritten rows before any fragment load.  Returns false if the wait
+// ran out (the rows are then left as they are).
+__device__ bool stage_to_f16(const DecodeCtx& cx, int32_t ph, uint64_t* bar, float* rowscale, int warp, int lane,
+                             int nwarps, int nthreads) {
+  bool ok = mbar_wait_sleep(bar, (uint32_t)ph, cx.a.err);
+  ok = !__any_sync(0xffffffffu, !ok);
+  const int32_t* sb = ph ? cx.sbd : cx.sbu;
+  const int32_t span = ph ? cx.span_d : cx.span_u;
+  const int32_t rows = span > 0 ? sb[span] : 0;
+  const int32_t n8 = (ph ? cx.a.I : cx.a.H) / 8;
+  const uint32_t RS = ph ? cx.RSd : cx.RSu;
+  for (int32_t r = warp; ok && r < rows; r += nwarps) {
+    uint4* row = reinterpret_cast<uint4*>(cx.stage + (size_t)r * RS);
+    uint32_t mx = 0;
+    for (int32_t i = lane; i < n8; i += 32) {
+      const uint4 v = row[i];
+      mx = bf16x2_absmax(v.x, bf16x2_absmax(v.y, bf16x2_absmax(v.z, bf16x2_absmax(v.w, mx))));
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, d));
+    // floor(log2) of the largest magnitude: the bf16 exponent, or for a
+    // subnormal (value m * 2^-133) the top bit of its mantissa
+    const int32_t lg = (mx >> 7) ? (int32_t)(mx >> 7) - 127 : (31 - __clz((int)mx)) - 133;
+    const int32_t s = mx ? min(126, max(-126, lg - 14)) : 0;
+    const float down = __uint_as_float((uint32_t)(127 - s) << 23);
+    if (lane == 0) rowscale[r] = __uint_as_float((uint32_t)(127 + s) << 23);
+    for (int32_t i = lane; i < n8; i += 32) {
+      const uint4 v = row[i];
+      row[i] = make_uint4(bf16x2_to_f16x2_scaled(v.x, down), bf16x2_to_f16x2_scaled(v.y, down),
+                          bf16x2_to_f16x2_scaled(v.z, down), bf16x2_to_f16x2_scaled(v.w, down));
+    }
+  }
+  all_warps_sync(nthreads);
+  return ok;
+}
+
 // One warp from its ring fill through the grid barrier to the drain of its
 // copies.  STAGED: the activation fragments come from the CTA-wide stage,
 // otherwise from each chunk's own activation copies (compiled separately so
@@ -732,9 +903,9 @@ __device__ __forceinline__ void combine_one(const DecodeArgs& a, const int32_t* 
 template <bool STAGED>
 __device__ __forceinline__ void decode_stream(const DecodeArgs& a, const DecodeCtx& cx, uint8_t* ring,
                                               uint32_t slot_bytes, int32_t P, uint64_t* wbar, Cur* wdesc,
-                                              uint64_t* stage_bar, const uint32_t* lut, float4* partial,
-                                              int32_t* pcount, const int32_t* s_inv, int32_t n_act, int tid,
-                                              int nthreads) {
+                                              uint64_t* stage_bar, const uint32_t* lut, const uint32_t* lut16,
+                                              float* rowscale, float4* partial, int32_t* pcount,
+                                              const int32_t* s_inv, int32_t n_act, int tid, int nthreads) {
   const int lane = tid & 31, warp = tid >> 5;
   const uint32_t wbytes = cx.wbytes;
   const uint64_t pol = policy_evict_first();
@@ -762,7 +933,7 @@ __device__ __forceinline__ void decode_stream(const DecodeArgs& a, const DecodeC
   // The up phase's staged activation rows go first, then the rings fill in
   // rounds -- every warp's first chunk, then every warp's second, ... -- so
   // that the copies needed first lead the SM's copy queue.
-  int32_t stage_issued = 0, stage_seen = 0;
+  int32_t stage_issued = 0;
   if (STAGED && warp == 0) {
     cx.issue_stage(0, lane, stage_bar);
     stage_issued = 1;
@@ -771,20 +942,28 @@ __device__ __forceinline__ void decode_stream(const DecodeArgs& a, const DecodeC
     if (ci.ph < 2) issue(s);
     all_warps_sync(nthreads);
   }
+  // staged rows become scaled f16 rows once they land (every warp helps)
+  if (STAGED && !stage_to_f16(cx, 0, stage_bar, rowscale, warp, lane, nthreads >> 5, nthreads)) dead = true;
 
   int32_t consumed = 0, slot = 0;
   uint32_t phase = 0;
   float accA[4] = {0.f, 0.f, 0.f, 0.f}, accA2[4] = {0.f, 0.f, 0.f, 0.f};
   float accB[4] = {0.f, 0.f, 0.f, 0.f}, accB2[4] = {0.f, 0.f, 0.f, 0.f};
-  while (consumed < issued) {
+  while (!dead && consumed < issued) {
     const Cur cur = wdesc[slot];
     if (cur.ph == 1 && !crossed) {
       // every up tile of every CTA is stored before any down tile reads Ap
       decode_grid_barrier(a, tid, nthreads);
       crossed = true;
-      if (STAGED && warp == 0) {
-        cx.issue_stage(1, lane, stage_bar);
-        stage_issued = 2;
+      if (STAGED) {
+        if (warp == 0) {
+          cx.issue_stage(1, lane, stage_bar);
+          stage_issued = 2;
+        }
+        if (!stage_to_f16(cx, 1, stage_bar, rowscale, warp, lane, nthreads >> 5, nthreads)) {
+          dead = true;
+          break;
+        }
       }
       for (int32_t q = acts_issued; q < issued; ++q) {
         const int32_t s = q % P;
@@ -792,12 +971,7 @@ __device__ __forceinline__ void decode_stream(const DecodeArgs& a, const DecodeC
       }
       acts_issued = issued;
     }
-    bool ok = mbar_wait_sleep(&wbar[slot], phase, a.err);
-    if (STAGED && ok && stage_seen <= cur.ph) {
-      // the stage's phase cur.ph is the CTA barrier's phase of the same number
-      ok = mbar_wait_sleep(stage_bar, (uint32_t)cur.ph, a.err);
-      stage_seen = cur.ph + 1;
-    }
+    const bool ok = mbar_wait_sleep(&wbar[slot], phase, a.err);
     if (__any_sync(0xffffffffu, !ok)) {
       dead = true;
       break;
@@ -806,7 +980,7 @@ __device__ __forceinline__ void decode_stream(const DecodeArgs& a, const DecodeC
       // once the first chunk has landed, ask L2 for the chunks past the ring
       Cur cp = ci;
       for (int q = 0; q < kDecL2Ahead && cp.ph < 2; ++q) {
-        const uint8_t* src = cx.chunk_src(cp);
+        const uint8_t* src = cx.template chunk_src<STAGED>(cp);
         prefetch_l2_bulk(src, (uint32_t)cx.kts(cp) * kTileBytes);
         if (cx.two(cp))
           prefetch_l2_bulk(src + (size_t)(cp.ph ? cx.KTd : cx.KTu) * kTileBytes, (uint32_t)cx.kts(cp) * kTileBytes);
@@ -819,7 +993,10 @@ __device__ __forceinline__ void decode_stream(const DecodeArgs& a, const DecodeC
     const uint8_t* act =
         STAGED ? cx.stage + (size_t)(cur.srow + col) * (cur.ph ? cx.RSd : cx.RSu) + cur.kt * 128 + (lane & 3) * 32
                : sp + wbytes + col * kDecActRow + (lane & 3) * 32;
-    chunk_mma(sp, act, cx.kts(cur), cx.two(cur), lane, lut, accA, accA2, accB, accB2);
+    if (STAGED)
+      chunk_mma16(sp, act, cx.kts(cur), cx.two(cur), lane, lut16, accA, accA2, accB, accB2);
+    else
+      chunk_mma(sp, act, cx.kts(cur), cx.two(cur), lane, lut, accA, accA2, accB, accB2);
     ++consumed;
     __syncwarp();
     if (ci.ph < 2) {
@@ -839,14 +1016,17 @@ __device__ __forceinline__ void decode_stream(const DecodeArgs& a, const DecodeC
         v[4 + q] = accB[q] + accB2[q];
         accA[q] = accA2[q] = accB[q] = accB2[q] = 0.f;
       }
-      decode_epilogue(cx, cur, v, lane, partial, pcount, s_inv, n_act);
+      decode_epilogue(cx, cur, v, lane, partial, pcount, s_inv, n_act, STAGED ? rowscale : nullptr);
     }
   }
   if (!crossed) {
     decode_grid_barrier(a, tid, nthreads);
-    if (STAGED && warp == 0) {
-      cx.issue_stage(1, lane, stage_bar);
-      stage_issued = 2;
+    if (STAGED) {
+      if (warp == 0) {
+        cx.issue_stage(1, lane, stage_bar);
+        stage_issued = 2;
+      }
+      if (!stage_to_f16(cx, 1, stage_bar, rowscale, warp, lane, nthreads >> 5, nthreads)) dead = true;
     }
   }
   if (stage_issued > 0) {
@@ -874,6 +1054,8 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) decode_kernel(const __gr
   extern __shared__ __align__(1024) uint8_t smem[];
   const DecLayout& L = a.L;
   uint32_t* lut = reinterpret_cast<uint32_t*>(smem + L.scale_lut);
+  uint32_t* lut16 = reinterpret_cast<uint32_t*>(smem + L.scale_lut16);
+  float* rowscale = reinterpret_cast<float*>(smem + L.rowexp);
   int32_t* s_ids = reinterpret_cast<int32_t*>(smem + L.ids);
   int32_t* s_tok = reinterpret_cast<int32_t*>(smem + L.perm);
   int32_t* s_inv = reinterpret_cast<int32_t*>(smem + L.inv);
@@ -911,12 +1093,16 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) decode_kernel(const __gr
         int64_t len = per - off < hi - lo ? per - off : hi - lo;
         len = len < 65536 ? len : 65536;
         const int32_t e = __ldg(a.ids + j);
-        if (e >= 0 && e < E && len >= 16) prefetch_l2_bulk(a.up_tiles + (size_t)e * per + off, (uint32_t)(len & ~int64_t(15)));
+        // (batches of several tokens mostly stream the f16 path's tiles)
+        const uint8_t* tiles = CAN_STAGE ? a.up_tiles16 : a.up_tiles;
+        if (e >= 0 && e < E && len >= 16) prefetch_l2_bulk(tiles + (size_t)e * per + off, (uint32_t)(len & ~int64_t(15)));
         lo += len;
       }
     }
   }
   for (int i = tid; i < 256; i += nthreads) lut[i] = scale_bf16_2p118((uint32_t)i) * 0x10001u;
+  if (CAN_STAGE)
+    for (int i = tid; i < 256; i += nthreads) lut16[i] = scale_f16x2((uint32_t)i);
   for (int i = tid; i < kDecMaxWarps; i += nthreads) pcount[i] = 0;
   if (lane == 0) {
     // one arrival: lane 0's expect_tx covering the weight and activation copies
@@ -997,11 +1183,11 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) decode_kernel(const __gr
   uint64_t* wbar = bars + warp * kDecMaxSlots;
   Cur* wdesc = descs + warp * kDecMaxSlots;
   if (CAN_STAGE && staged)
-    decode_stream<true>(a, cx, ring, slot_bytes, P, wbar, wdesc, stage_bar, lut, partial, pcount, s_inv, n_act,
-                        tid, nthreads);
+    decode_stream<true>(a, cx, ring, slot_bytes, P, wbar, wdesc, stage_bar, lut, lut16, rowscale, partial, pcount,
+                        s_inv, n_act, tid, nthreads);
   else
-    decode_stream<false>(a, cx, ring, slot_bytes, P, wbar, wdesc, stage_bar, lut, partial, pcount, s_inv, n_act,
-                         tid, nthreads);
+    decode_stream<false>(a, cx, ring, slot_bytes, P, wbar, wdesc, stage_bar, lut, lut16, rowscale, partial, pcount,
+                         s_inv, n_act, tid, nthreads);
   if (!a.ext && a.n > kDecLateCombine) {
     // every down row of every CTA is stored: combine, one element per thread
     decode_grid_barrier(a, tid, nthreads);

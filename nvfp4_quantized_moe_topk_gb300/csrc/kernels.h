@@ -132,7 +132,8 @@ constexpr int kDecMaxTokens = 64;      // and tokens run as one launch
 
 // Shared-memory plan of the decode kernel (byte offsets; the host computes it).
 struct DecLayout {
-  uint32_t scale_lut, ids, perm, inv, counts, offsets, act, misc, bars, partial, pcount, desc, sbase, ring, total;
+  uint32_t scale_lut, scale_lut16, ids, perm, inv, counts, offsets, act, misc, bars, partial, pcount, desc, sbase,
+      rowexp, ring, total;
   uint32_t warps;
 };
 
@@ -146,6 +147,7 @@ inline DecLayout dec_layout(int32_t E, int32_t R, uint32_t budget) {
     return at;
   };
   L.scale_lut = take(256 * 4, 128);
+  L.scale_lut16 = take(256 * 4, 128);
   L.ids = take(4 * (uint32_t)R, 16);
   L.perm = take(4 * (uint32_t)R, 16);
   L.inv = take(4 * (uint32_t)R, 16);
@@ -158,6 +160,7 @@ inline DecLayout dec_layout(int32_t E, int32_t R, uint32_t budget) {
   L.pcount = take(kDecMaxWarps * 4, 16);
   L.desc = take(kDecMaxWarps * kDecMaxSlots * 48, 16);  // per-slot chunk descriptors
   L.sbase = take(4 * 2 * (kDecMaxSpan + 1), 16);        // per phase: first stage row of each staged expert
+  L.rowexp = take(4 * kDecPassTok * kDecMaxSpan, 16);   // power-of-two exponent of each staged row
   const uint32_t ring_at = (o + 127) / 128 * 128;
   uint32_t warps = budget > ring_at ? (budget - ring_at) / (2 * kDecSlotBytes) : 0;
   if (warps > (uint32_t)kDecMaxWarps) warps = kDecMaxWarps;
@@ -170,6 +173,8 @@ inline DecLayout dec_layout(int32_t E, int32_t R, uint32_t budget) {
 struct DecodeArgs {
   const uint8_t* up_tiles;    // [E][I/16][H/64][576]; gated: [E][2I/16][H/64][576], gate and up tiles alternating
   const uint8_t* dn_tiles;    // [E][H/16][I/64][576]
+  const uint8_t* up_tiles16;  // the same tiles with codes in byte order for the f16 path (launch_repack_frag16)
+  const uint8_t* dn_tiles16;
   const float* up_g;
   const float* dn_g;
   const float* gate_g;        // gated only
@@ -198,6 +203,8 @@ struct DecodeArgs {
 
 cudaError_t launch_repack_frag(const uint8_t* codes, const uint8_t* scales, int32_t G, int32_t N, int32_t K,
                                uint8_t* out, cudaStream_t s);
+cudaError_t launch_repack_frag16(const uint8_t* codes, const uint8_t* scales, int32_t G, int32_t N, int32_t K,
+                                 uint8_t* out, cudaStream_t s);
 // Shared-memory plan for E experts and R pairs (227 KB budget).
 DecLayout decode_layout(int32_t E, int32_t R);
 cudaError_t launch_decode(const DecodeArgs& args, int num_sms, cudaStream_t s);
