@@ -723,8 +723,8 @@ __device__ __forceinline__ void decode_epilogue(const DecodeCtx& cx, const Cur& 
     const int32_t first_item = ra / KT;
     const int32_t seg_lo = cur.i == first_item ? ra - cur.i * KT : 0;
     if (seg_lo != 0 || cur.kt_end != KT) {
-      const int64_t TT = (int64_t)(up ? cx.n_up : cx.n_dn) * KT;
-      const int64_t Wp = up ? cx.Wu : cx.Wd;
+      const uint32_t TT = (uint32_t)(up ? cx.n_up : cx.n_dn) * (uint32_t)KT;  // below 2^32 with x16
+      const uint32_t Wp = (uint32_t)(up ? cx.Wu : cx.Wd);
       const int32_t side = cur.i == first_item ? 0 : 1;
       float4* slot = partial + ((cx.warp * 2 + side) * 32 + lane) * 2;
       slot[0] = make_float4(v[0], v[1], v[2], v[3]);
@@ -732,8 +732,8 @@ __device__ __forceinline__ void decode_epilogue(const DecodeCtx& cx, const Cur& 
       __threadfence_block();
       __syncwarp();
       // warps holding tile rows i*KT .. (i+1)*KT-1 of this phase
-      const int32_t wf = (int32_t)((((int64_t)cur.i * KT + 1) * Wp - 1) / TT);
-      const int32_t wl = (int32_t)((((int64_t)(cur.i + 1) * KT) * Wp - 1) / TT);
+      const int32_t wf = (int32_t)((((uint32_t)cur.i * KT + 1) * Wp - 1) / TT);
+      const int32_t wl = (int32_t)((((uint32_t)(cur.i + 1) * KT) * Wp - 1) / TT);
       int32_t last = 0;
       if (lane == 0) {
         last = atomicAdd(&pcount[wf], 1) == wl - wf;
@@ -744,7 +744,7 @@ __device__ __forceinline__ void decode_epilogue(const DecodeCtx& cx, const Cur& 
       __threadfence_block();
       float4 rA = make_float4(0.f, 0.f, 0.f, 0.f), rB = rA;
       for (int32_t w2 = wf; w2 <= wl; ++w2) {
-        const int32_t fi = (int32_t)((TT * w2) / Wp) / KT;
+        const int32_t fi = (int32_t)((TT * (uint32_t)w2) / Wp) / KT;
         const float4* u = partial + ((w2 * 2 + (cur.i == fi ? 0 : 1)) * 32 + lane) * 2;
         rA.x += u[0].x; rA.y += u[0].y; rA.z += u[0].z; rA.w += u[0].w;
         rB.x += u[1].x; rB.y += u[1].y; rB.z += u[1].z; rB.w += u[1].w;
@@ -1082,20 +1082,21 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) decode_kernel(const __gr
     // While the routing is worked out, ask L2 for the up weights of the picked
     // experts (a slice per CTA of their concatenation in pair order), when
     // they fit well inside L2: the ring's first requests then find them there.
-    const int64_t per = (int64_t)((a.gated ? 2 * a.I : a.I) / 16) * (a.H / 64) * kTileBytes;
-    const int64_t total = (int64_t)R * per;
-    if (total <= kDecEarlyL2Bytes) {
-      int64_t lo = (total * blockIdx.x / gridDim.x) & ~int64_t(15);
-      const int64_t hi = (total * (blockIdx.x + 1) / gridDim.x) & ~int64_t(15);
+    // (32-bit arithmetic once the total is known to be below 48 MB: this
+    // thread's divisions would otherwise hold up the CTA's first barrier)
+    const uint32_t per = (uint32_t)((a.gated ? 2 * a.I : a.I) / 16) * (uint32_t)(a.H / 64) * kTileBytes;
+    if ((int64_t)R * per <= kDecEarlyL2Bytes) {
+      const uint32_t total = (uint32_t)R * per;
+      const uint32_t share = ((total + gridDim.x - 1) / gridDim.x + 15u) & ~15u;
+      uint32_t lo = blockIdx.x * share;
+      const uint32_t hi = min(total, lo + share);
+      // (batches of several tokens mostly stream the f16 path's tiles)
+      const uint8_t* tiles = CAN_STAGE ? a.up_tiles16 : a.up_tiles;
       while (lo < hi) {
-        const int32_t j = (int32_t)(lo / per);
-        const int64_t off = lo - (int64_t)j * per;
-        int64_t len = per - off < hi - lo ? per - off : hi - lo;
-        len = len < 65536 ? len : 65536;
+        const uint32_t j = lo / per, off = lo - j * per;
+        const uint32_t len = min(min(per - off, hi - lo), 65536u);
         const int32_t e = __ldg(a.ids + j);
-        // (batches of several tokens mostly stream the f16 path's tiles)
-        const uint8_t* tiles = CAN_STAGE ? a.up_tiles16 : a.up_tiles;
-        if (e >= 0 && e < E && len >= 16) prefetch_l2_bulk(tiles + (size_t)e * per + off, (uint32_t)(len & ~int64_t(15)));
+        if (e >= 0 && e < E && len >= 16) prefetch_l2_bulk(tiles + (size_t)e * per + off, len & ~15u);
         lo += len;
       }
     }
@@ -1171,13 +1172,15 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) decode_kernel(const __gr
     cx.n_up = it.n_up;
     cx.n_dn = it.n_dn;
     cx.split = cmax <= kDecPassTok;
-    const int64_t TTu = (int64_t)cx.n_up * cx.KTu, TTd = (int64_t)cx.n_dn * cx.KTd;
-    cx.Wu = (int32_t)(TTu < Weff ? TTu : Weff);
-    cx.Wd = (int32_t)(TTd < Weff ? TTd : Weff);
-    cx.ura = warp < cx.Wu ? (int32_t)(TTu * warp / cx.Wu) : 0;
-    cx.urb = warp < cx.Wu ? (int32_t)(TTu * (warp + 1) / cx.Wu) : 0;
-    cx.dra = warp < cx.Wd ? (int32_t)(TTd * warp / cx.Wd) : 0;
-    cx.drb = warp < cx.Wd ? (int32_t)(TTd * (warp + 1) / cx.Wd) : 0;
+    // k-tiles per phase and CTA: at most 262144 items (E <= 1024, 256 per
+    // expert) x 64 k-tiles, times at most 16 warps, stays below 2^32
+    const uint32_t TTu = (uint32_t)cx.n_up * (uint32_t)cx.KTu, TTd = (uint32_t)cx.n_dn * (uint32_t)cx.KTd;
+    cx.Wu = (int32_t)(TTu < (uint32_t)Weff ? TTu : (uint32_t)Weff);
+    cx.Wd = (int32_t)(TTd < (uint32_t)Weff ? TTd : (uint32_t)Weff);
+    cx.ura = warp < cx.Wu ? (int32_t)(TTu * (uint32_t)warp / (uint32_t)cx.Wu) : 0;
+    cx.urb = warp < cx.Wu ? (int32_t)(TTu * (uint32_t)(warp + 1) / (uint32_t)cx.Wu) : 0;
+    cx.dra = warp < cx.Wd ? (int32_t)(TTd * (uint32_t)warp / (uint32_t)cx.Wd) : 0;
+    cx.drb = warp < cx.Wd ? (int32_t)(TTd * (uint32_t)(warp + 1) / (uint32_t)cx.Wd) : 0;
   }
   uint8_t* ring = smem + L.ring + (size_t)min(warp, Weff - 1) * P * slot_bytes;
   uint64_t* wbar = bars + warp * kDecMaxSlots;
