@@ -82,3 +82,53 @@ def test_staged_and_per_chunk_ctas_in_one_launch(dev, gated):
     again = run_forward(layer, wl, dev)
     assert np.array_equal(got, again), "repeated forward changed bits"
     layer.close()
+
+
+def _scale_rows_pow2(bits, exps):
+    """bf16 rows times 2^exps[row], exactly (the values stay normal bf16)."""
+    v = W.bf16_bits_to_f32(bits).astype(np.float64) * np.ldexp(1.0, np.asarray(exps))[:, None]
+    out = W.f32_to_bf16_bits(v.astype(np.float32))
+    assert np.array_equal(W.bf16_bits_to_f32(out).astype(np.float64), v), "scaling must be exact"
+    return out
+
+
+@pytest.mark.parametrize("gated", [False, True])
+def test_staged_f16_rows_across_the_bf16_range(dev, gated):
+    """The staged path computes in f16 after scaling each activation row by a
+    power of two; rows 2^-40 .. 2^50 (their relu^2 / silu * up rows spanning
+    roughly 2^-75 .. 2^105) would leave f16's range without that scaling.
+    One row also holds values 2^-36 below the rest, which land among f16's
+    subnormals.  Each token's output, and each packed row's intermediate and
+    down row, is held to the layer bound against its own RMS."""
+    import torch
+
+    wl = W.small_custom(8, 512, 256, 4, 2, seed=72, gated=gated, scales="full", globals_="distinct")
+    exps = np.array([-40, -24, -8, 0, 8, 16, 24, 36])
+    wl.x = _scale_rows_pow2(wl.x, exps)
+    x0 = W.bf16_bits_to_f32(wl.x).astype(np.float64)
+    x0[0, ::7] *= 2.0 ** -36
+    wl.x = W.f32_to_bf16_bits(x0.astype(np.float32))
+    wl.dst = _scale_rows_pow2(wl.dst, exps)
+    counts = np.bincount(wl.topk_ids.ravel(), minlength=wl.E)
+    assert counts.max() <= 8
+    layer = make_layer(wl, dev)
+    got = run_forward(layer, wl, dev)
+    assert layer.device_error() == 0
+    ref = oracle.moe_forward(wl, intermediates=True, out_f64=True)
+    a = torch.empty((wl.R, wl.I), dtype=torch.int16, device=dev)
+    y = torch.empty((wl.R, wl.H), dtype=torch.float32, device=dev)
+    layer.debug_intermediates(a, y)
+    torch.cuda.synchronize()
+    a = a.cpu().numpy().view(np.uint16)
+    y = y.cpu().numpy()
+    layer.close()
+    assert np.all(np.isfinite(W.bf16_bits_to_f32(got)))
+    e_rows, extra_out = flip_allowance(wl, a, ref.a_rows)
+    for r in range(wl.R):
+        ok_a, ea, ra = layer_tolerance_check(a, ref.a_f64, rows=[r])
+        assert ok_a, f"packed row {r}: intermediate max|err| {ea:.4g} vs rms {ra:.4g}"
+        ok_y, ey, ry = fp_tolerance_check(y[r:r + 1], ref.y_rows[r:r + 1], extra=e_rows[r:r + 1])
+        assert ok_y, f"packed row {r}: down row max|err| {ey:.4g} vs rms {ry:.4g}"
+    for t in range(wl.n):
+        ok, err, rms = layer_tolerance_check(got, ref.out_f64, rows=[t], extra=extra_out)
+        assert ok, f"token {t} (x 2^{exps[t]}): output max|err| {err:.4g} vs rms {rms:.4g}"
