@@ -84,6 +84,7 @@ struct moe_nvfp4 {
   // and in packed 128-row blocks for the grouped GEMM
   uint8_t *up_blocks = nullptr, *dn_blocks = nullptr;
   int32_t *col_done = nullptr, *grid_bar = nullptr;
+  float4* dec_partial = nullptr;  // streaming kernel: split-item partial sums, per CTA
   // workspace (max_tokens)
   int32_t *counts = nullptr, *offsets = nullptr, *perm_pair = nullptr, *inv = nullptr, *err = nullptr;
   int32_t* blk_hist = nullptr;  // per-slice expert histograms of the routing kernels
@@ -124,7 +125,7 @@ void free_handle(moe_nvfp4* h) {
                   h->counts,   h->offsets,   h->perm_pair, h->inv,      h->err,       h->Xp,
                   h->Ap,       h->Yp,        h->x_stage,   h->dst_stage, h->ids_stage, h->w_stage,
                   h->up_tiles, h->dn_tiles,  h->col_done,  h->grid_bar,  h->up_blocks, h->dn_blocks,
-                  h->up_tiles16, h->dn_tiles16,
+                  h->up_tiles16, h->dn_tiles16, h->dec_partial,
                   h->gate_codes, h->gate_scales, h->gate_g, h->blk_hist, h->dense_ids, h->dense_w};
   for (void* p : ptrs)
     if (p) cudaFree(p);
@@ -294,6 +295,7 @@ moe_status moe_nvfp4_create(const moe_nvfp4_config* config, const moe_nvfp4_weig
   TRY(cudaMalloc(&h->dn_blocks, gemm_blocks_bytes((int32_t)E, (int32_t)H, (int32_t)I)));
   TRY(cudaMalloc(&h->col_done, (H / 16) * sizeof(int32_t)));
   TRY(cudaMalloc(&h->grid_bar, 2 * sizeof(int32_t)));
+  TRY(cudaMalloc(&h->dec_partial, (size_t)h->num_sms * kDecPartialPerCta * sizeof(float4)));
   TRY(cudaMemcpyAsync(h->up_codes, w->up_codes, mat_codes, cudaMemcpyDeviceToDevice, s));
   TRY(cudaMemcpyAsync(h->dn_codes, w->down_codes, mat_codes, cudaMemcpyDeviceToDevice, s));
   TRY(cudaMemcpyAsync(h->up_scales, w->up_scales, mat_scales, cudaMemcpyDeviceToDevice, s));
@@ -403,6 +405,7 @@ static moe_status forward_impl(moe_nvfp4* h, const uint16_t* x, const int32_t* i
   d.g_perm = h->perm_pair;
   d.g_inv = h->inv;
   d.col_done = h->col_done;
+  d.partial = h->dec_partial;
   d.grid_bar = h->grid_bar;
   d.err = h->err;
   d.n = n;
@@ -412,7 +415,7 @@ static moe_status forward_impl(moe_nvfp4* h, const uint16_t* x, const int32_t* i
   d.k = k;
   if (n <= h->single_max_tokens && R <= kDecMaxPairs) {
     // the whole layer in one launch
-    d.L = decode_layout(E, R);
+    d.L = decode_layout(E, R, decode_can_stage(n, 0));
     if (d.L.warps >= 4) {
       if (dst_ready && cudaStreamWaitEvent(s, dst_ready, 0) != cudaSuccess) return MOE_ERR_CUDA;
       if (dst_out) {
@@ -440,7 +443,7 @@ static moe_status forward_impl(moe_nvfp4* h, const uint16_t* x, const int32_t* i
   if (gemm) {
     d.ext = 1;
     d.max_rows = h->threshold;
-    d.L = decode_layout(E, 0);
+    d.L = decode_layout(E, 0, true);
     if (d.L.warps >= 4) {
       TimedLaunch tl(h, s, kKSmall);
       e = launch_decode(d, h->num_sms, s);

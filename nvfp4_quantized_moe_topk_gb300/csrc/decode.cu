@@ -729,7 +729,7 @@ __device__ __forceinline__ void decode_epilogue(const DecodeCtx& cx, const Cur& 
       float4* slot = partial + ((cx.warp * 2 + side) * 32 + lane) * 2;
       slot[0] = make_float4(v[0], v[1], v[2], v[3]);
       slot[1] = make_float4(v[4], v[5], v[6], v[7]);
-      __threadfence_block();
+      __threadfence_block();  // the readers are warps of this CTA (shared or L1-coherent global memory)
       __syncwarp();
       // warps holding tile rows i*KT .. (i+1)*KT-1 of this phase
       const int32_t wf = (int32_t)((((uint32_t)cur.i * KT + 1) * Wp - 1) / TT);
@@ -1066,7 +1066,8 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) decode_kernel(const __gr
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* stage_bar = bars + kDecMaxSlots * kDecMaxWarps;
   int32_t* s_sbase = reinterpret_cast<int32_t*>(smem + L.sbase);
-  float4* partial = reinterpret_cast<float4*>(smem + L.partial);
+  float4* partial = CAN_STAGE ? a.partial + (size_t)blockIdx.x * kDecPartialPerCta
+                              : reinterpret_cast<float4*>(smem + L.partial);
   int32_t* pcount = reinterpret_cast<int32_t*>(smem + L.pcount);
   Cur* descs = reinterpret_cast<Cur*>(smem + L.desc);
 
@@ -1200,11 +1201,13 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) decode_kernel(const __gr
   }
 }
 
-DecLayout decode_layout(int32_t E, int32_t R) { return dec_layout(E, R, 227 * 1024 - 1024); }
+DecLayout decode_layout(int32_t E, int32_t R, bool can_stage) {
+  return dec_layout(E, R, 227 * 1024 - 1024, !can_stage);
+}
 
 cudaError_t launch_decode(const DecodeArgs& args, int num_sms, cudaStream_t s) {
   static std::atomic<bool> attr_set[2][kMaxDevices];
-  const bool can_stage = args.n > 1 || args.ext;
+  const bool can_stage = decode_can_stage(args.n, args.ext);
   auto kernel = can_stage ? decode_kernel<true> : decode_kernel<false>;
   cudaError_t e = raise_smem_limit(kernel, 227 * 1024, attr_set[can_stage ? 1 : 0]);
   if (e != cudaSuccess) return e;

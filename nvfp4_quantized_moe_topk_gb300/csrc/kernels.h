@@ -125,6 +125,11 @@ constexpr int kDecPassTok = 8;         // tokens per pass over a tile (one n8 MM
 constexpr int kDecL2Ahead = 8;         // chunks past the ring requested into L2 at start
 constexpr long long kDecEarlyL2Bytes = 48ll << 20;  // picked experts' up weights prefetched during routing, at most
 constexpr int kDecLateCombine = 8;     // larger batches combine after a second grid barrier
+// Partial sums of split items, per CTA: (warp, first/last segment) x 32 lanes x
+// 2 float4.  The kernel that can stage keeps them in global memory (an
+// L1-resident 32 KB per SM) so that the shared memory goes to the ring and
+// the stage; the one-token kernel keeps them in shared memory.
+constexpr int kDecPartialPerCta = 2 * kDecMaxWarps * 32 * 2;  // float4
 constexpr int kDecMaxSpan = 16;        // experts whose activation rows one CTA stages per phase, at most
 constexpr int kDecStageMax = 96 * 1024;  // bytes of staged activation rows per CTA, at most
 constexpr int kDecMaxPairs = 1024;     // batches with at most this many pairs
@@ -137,7 +142,7 @@ struct DecLayout {
   uint32_t warps;
 };
 
-inline DecLayout dec_layout(int32_t E, int32_t R, uint32_t budget) {
+inline DecLayout dec_layout(int32_t E, int32_t R, uint32_t budget, bool smem_partial) {
   DecLayout L{};
   uint32_t o = 0;
   auto take = [&](uint32_t bytes, uint32_t align) {
@@ -156,7 +161,7 @@ inline DecLayout dec_layout(int32_t E, int32_t R, uint32_t budget) {
   L.act = take(4 * (uint32_t)E, 16);
   L.misc = take(64, 16);
   L.bars = take(8 * (kDecMaxSlots * kDecMaxWarps + 1), 16);  // ring slots, then the stage barrier
-  L.partial = take(2 * kDecMaxWarps * 32 * 32, 128);  // (warp, first/last segment) x lanes x 2 float4
+  L.partial = smem_partial ? take(kDecPartialPerCta * 16, 128) : 0;
   L.pcount = take(kDecMaxWarps * 4, 16);
   L.desc = take(kDecMaxWarps * kDecMaxSlots * 48, 16);  // per-slot chunk descriptors
   L.sbase = take(4 * 2 * (kDecMaxSpan + 1), 16);        // per phase: first stage row of each staged expert
@@ -191,6 +196,7 @@ struct DecodeArgs {
   int32_t* g_perm;
   int32_t* g_inv;
   int32_t* col_done;          // [H/16] combine counters, zero between launches
+  float4* partial;            // [gridDim.x][kDecPartialPerCta] split-item partial sums (scratch)
   int32_t* grid_bar;          // 8-byte aligned: one 64-bit arrival count (multiple of the grid between launches)
   int32_t* err;
   int32_t n, H, I, E, k;
@@ -205,8 +211,12 @@ cudaError_t launch_repack_frag(const uint8_t* codes, const uint8_t* scales, int3
                                uint8_t* out, cudaStream_t s);
 cudaError_t launch_repack_frag16(const uint8_t* codes, const uint8_t* scales, int32_t G, int32_t N, int32_t K,
                                  uint8_t* out, cudaStream_t s);
-// Shared-memory plan for E experts and R pairs (227 KB budget).
-DecLayout decode_layout(int32_t E, int32_t R);
+// Shared-memory plan for E experts and R pairs (227 KB budget), for the
+// kernel launch_decode picks for these arguments.
+DecLayout decode_layout(int32_t E, int32_t R, bool can_stage);
+// The streaming kernel that can stage activation rows (several tokens, or
+// external routing); one-token batches take the per-chunk kernel alone.
+inline bool decode_can_stage(int32_t n, int32_t ext) { return n > 1 || ext; }
 cudaError_t launch_decode(const DecodeArgs& args, int num_sms, cudaStream_t s);
 
 // Host helpers for tensor maps (driver entry point resolved at run time).
