@@ -82,7 +82,8 @@ constexpr uint32_t bars = scale_lut + 256 * 4;
 constexpr uint32_t misc = bars + nbars * 8;
 constexpr uint32_t tile_start = misc + 64;
 constexpr uint32_t group_id = tile_start + (kMaxGroups + 1) * 4;
-constexpr uint32_t end = group_id + kMaxGroups * 4;
+constexpr uint32_t part_start = group_id + kMaxGroups * 4;
+constexpr uint32_t end = part_start + (kMaxGroups + 1) * 4;
 constexpr uint32_t alloc = end + 1024;
 }  // namespace g2
 
@@ -184,21 +185,40 @@ struct G2Tile {
   int32_t g, row0, rows, n0;
 };
 
-__device__ __forceinline__ G2Tile g2_tile(int32_t t, const int32_t* tile_start, const int32_t* group_id,
-                                          int32_t ngroups, const Gemm2Args& a, int32_t nb) {
+// Tile t: the full token tiles of every selected group come first (t < n_full,
+// group order, feature blocks fastest), then each group's last, partial token
+// tile.  A partial tile costs less than a full one, so the round-robin over
+// CTAs leaves the cheap tiles for the last rounds, where they even out the
+// CTAs' totals instead of adding to the longest.
+__device__ __forceinline__ int g2_last_group_at(const int32_t* start, int32_t ngroups, int32_t t) {
   int lo = 0, hi = ngroups - 1;  // last selected group whose first tile <= t
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (tile_start[mid] <= t) lo = mid;
+    if (start[mid] <= t) lo = mid;
     else hi = mid - 1;
   }
+  return lo;
+}
+__device__ __forceinline__ G2Tile g2_tile(int32_t t, const int32_t* tile_start, const int32_t* part_start,
+                                          const int32_t* group_id, int32_t ngroups, int32_t n_full,
+                                          const Gemm2Args& a, int32_t nb) {
   G2Tile ti;
-  const int32_t local = t - tile_start[lo];
-  const int32_t mt = local / nb, ft = local - mt * nb;
-  ti.g = group_id[lo];
-  ti.row0 = a.offsets[ti.g] + mt * g2::kN;
-  ti.rows = min(g2::kN, a.counts[ti.g] - mt * g2::kN);
-  ti.n0 = ft * g2::kM;
+  if (t < n_full) {
+    const int i = g2_last_group_at(tile_start, ngroups, t);
+    const int32_t local = t - tile_start[i];
+    const int32_t mt = local / nb, ft = local - mt * nb;
+    ti.g = group_id[i];
+    ti.row0 = a.offsets[ti.g] + mt * g2::kN;
+    ti.rows = g2::kN;
+    ti.n0 = ft * g2::kM;
+  } else {
+    const int i = g2_last_group_at(part_start, ngroups, t - n_full);
+    ti.g = group_id[i];
+    const int32_t c = a.counts[ti.g], mt = c / g2::kN;
+    ti.row0 = a.offsets[ti.g] + mt * g2::kN;
+    ti.rows = c - mt * g2::kN;
+    ti.n0 = (t - n_full - part_start[i]) * g2::kM;
+  }
   return ti;
 }
 
@@ -255,6 +275,7 @@ __global__ void __launch_bounds__(g2::kThreads, 1)
   int32_t* total_sm = reinterpret_cast<int32_t*>(sm + g2::misc + 20);
   int32_t* tile_start = reinterpret_cast<int32_t*>(sm + g2::tile_start);
   int32_t* group_id = reinterpret_cast<int32_t*>(sm + g2::group_id);
+  int32_t* part_start = reinterpret_cast<int32_t*>(sm + g2::part_start);
   uint32_t* lut = reinterpret_cast<uint32_t*>(sm + g2::scale_lut);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -292,40 +313,50 @@ __global__ void __launch_bounds__(g2::kThreads, 1)
   pdl_wait();
 
   const int32_t nb = (a.N + g2::kM - 1) / g2::kM;
-  if (warp == 3) {  // tile list: selected groups in order, feature tiles fastest
-    int32_t run = 0, ng = 0;
+  if (warp == 3) {  // tile lists: selected groups in order, full token tiles, then the partial ones
+    int32_t run = 0, prun = 0, ng = 0;
     for (int base = 0; base < a.G; base += 32) {
       const int g = base + lane;
-      int32_t tiles = 0;
+      int32_t tiles = 0, ptiles = 0;
       bool sel = false;
       if (g < a.G) {
         const int32_t c = a.counts[g];
         sel = c > 0 && c > a.min_rows;
-        if (sel) tiles = ((c + g2::kN - 1) / g2::kN) * nb;
+        if (sel) {
+          tiles = (c / g2::kN) * nb;
+          ptiles = (c % g2::kN) ? nb : 0;
+        }
       }
       const uint32_t bal = __ballot_sync(0xffffffffu, sel);
-      int32_t incl = tiles;
+      int32_t incl = tiles, pincl = ptiles;
       for (int d = 1; d < 32; d <<= 1) {
         const int32_t v = __shfl_up_sync(0xffffffffu, incl, d);
-        if (lane >= d) incl += v;
+        const int32_t pv = __shfl_up_sync(0xffffffffu, pincl, d);
+        if (lane >= d) {
+          incl += v;
+          pincl += pv;
+        }
       }
       if (sel) {
         const int slot = ng + __popc(bal & ((1u << lane) - 1u));
         tile_start[slot] = run + incl - tiles;
+        part_start[slot] = prun + pincl - ptiles;
         group_id[slot] = g;
       }
       run += __shfl_sync(0xffffffffu, incl, 31);
+      prun += __shfl_sync(0xffffffffu, pincl, 31);
       ng += __popc(bal);
     }
     if (lane == 0) {
       *ngroups_sm = ng;
-      *total_sm = run;
+      *total_sm = run + prun;
+      *(total_sm + 1) = run;
     }
   }
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int32_t ngroups = *ngroups_sm, total_tiles = *total_sm;
+  const int32_t ngroups = *ngroups_sm, total_tiles = *total_sm, n_full = *(total_sm + 1);
   pdl_launch_dependents();
 
   const int32_t KB = a.K / g2::kK;
@@ -341,7 +372,7 @@ __global__ void __launch_bounds__(g2::kThreads, 1)
       uint32_t w_iss[g2::kWStages] = {}, b_iss[g2::kBStages] = {};
       bool ok = true;
       for (int32_t t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
-        const G2Tile ti = g2_tile(t, tile_start, group_id, ngroups, a, nb);
+        const G2Tile ti = g2_tile(t, tile_start, part_start, group_id, ngroups, n_full, a, nb);
         const uint8_t* wsrc = a.blocks + ((size_t)ti.g * nb + ti.n0 / g2::kM) * KB * (size_t)g2::kWBytes;
         for (int32_t kb = 0; kb < KB; ++kb) {
           if (!g2_wait(&w_empty[ws], wph ^ 1u, abort_flag, a.err)) {
@@ -402,7 +433,7 @@ __global__ void __launch_bounds__(g2::kThreads, 1)
     // offsets inside shared memory
     const uint64_t bdesc0 = smem_desc_k128(smem_u32(sm + g2::b));
     for (int32_t t = blockIdx.x; t < total_tiles && !done; t += gridDim.x, ++it) {
-      const G2Tile ti = g2_tile(t, tile_start, group_id, ngroups, a, nb);  // once per tile
+      const G2Tile ti = g2_tile(t, tile_start, part_start, group_id, ngroups, n_full, a, nb);  // once per tile
       const uint32_t acc = it & 1;
       const uint32_t ncols = (uint32_t)((ti.rows + 15) & ~15);
       const uint32_t idesc = idesc_bf16(g2::kM, ncols);
@@ -530,7 +561,7 @@ __global__ void __launch_bounds__(g2::kThreads, 1)
     const int row = 32 * q + lane;
     int it = 0;
     for (int32_t t = blockIdx.x; t < total_tiles; t += gridDim.x, ++it) {
-      const G2Tile ti = g2_tile(t, tile_start, group_id, ngroups, a, nb);
+      const G2Tile ti = g2_tile(t, tile_start, part_start, group_id, ngroups, n_full, a, nb);
       const uint32_t acc = it & 1, acc_phase = (it >> 1) & 1;
       if (!g2_wait(&tmem_full[acc], acc_phase, abort_flag, a.err)) break;
       tc_fence_after();
