@@ -211,8 +211,8 @@ int or_nvfp4_matmul(const uint16_t *A, const uint8_t *codes, const uint8_t *scal
 
 /* dst[i][c] = bf16_rne(dst[i][c] + sum_{j=0..k-1} w[i][j] * src[rows[i][j]][c]),
  * the terms added in increasing j (pull request #91, "What changes",
- * WeightedRowSum: a deterministic weighted sum of k source rows onto each dst
- * row, fixed j order, no atomics).  A row index outside [0, src_rows)
+ * WeightedRowSum: each dst row gets its k weighted source rows added in one
+ * set order, so the result does not depend on how the work is scheduled).  A row index outside [0, src_rows)
  * contributes nothing and is counted; the count is returned. */
 int64_t or_weighted_row_sum(uint16_t *dst, const double *src, const int32_t *rows, const float *w,
                             int64_t n, int k, int64_t cols, int64_t src_rows) {
