@@ -25,7 +25,12 @@
  *
  * NVFP4 weights: W[r][c] = e2m1(code[r][c]) * e4m3(scale[r][c/16]); the
  * per-matrix fp32 global g is applied to the product (the GEMM alpha), never
- * folded into the bf16 weights (same page, bf16 NVFP4 GEMM).
+ * folded into the bf16 weights (same page, bf16 NVFP4 GEMM).  Every product
+ * W * x is formed exactly: the weights are unpacked without rounding to bf16,
+ * or, where the small-batch kernel stages its activation rows (every expert
+ * holding at most 8 tokens), to f16 against activation rows rescaled by a
+ * power of two per row (exact for every value within 2^28 of its row's
+ * largest magnitude); the scale is undone on the fp32 sum.
  *
  * Conventions for every entry point:
  *   - All array arguments are plain pointers.  "device" means memory the GPU
