@@ -132,3 +132,34 @@ def test_staged_f16_rows_across_the_bf16_range(dev, gated):
     for t in range(wl.n):
         ok, err, rms = layer_tolerance_check(got, ref.out_f64, rows=[t], extra=extra_out)
         assert ok, f"token {t} (x 2^{exps[t]}): output max|err| {err:.4g} vs rms {rms:.4g}"
+
+
+@pytest.mark.parametrize("gated", [False, True])
+def test_staged_path_with_many_experts_per_cta(dev, gated):
+    """The single launch at its pair bound (64 tokens x top-16 = 1024 pairs)
+    over 1024 experts: every expert holds at most a few tokens, so CTAs stage,
+    each for five or six experts (small H and I: six or eight items per
+    expert).  Layer output and intermediates against the oracle."""
+    import torch
+
+    wl = W.small_custom(64, 256, 192, 1024, 16, seed=73, gated=gated, scales="full", globals_="distinct")
+    counts = np.bincount(wl.topk_ids.ravel(), minlength=wl.E)
+    assert wl.R == 1024 and 2 <= counts.max() <= 8
+    layer = make_layer(wl, dev)
+    got = run_forward(layer, wl, dev)
+    assert layer.device_error() == 0
+    ref = oracle.moe_forward(wl, intermediates=True, out_f64=True)
+    a = torch.empty((wl.R, wl.I), dtype=torch.int16, device=dev)
+    y = torch.empty((wl.R, wl.H), dtype=torch.float32, device=dev)
+    layer.debug_intermediates(a, y)
+    torch.cuda.synchronize()
+    a = a.cpu().numpy().view(np.uint16)
+    y = y.cpu().numpy()
+    layer.close()
+    ok_a, ea, ra = layer_tolerance_check(a, ref.a_f64)
+    assert ok_a, f"intermediate rows: max|err| {ea:.4g} vs rms {ra:.4g}"
+    e_rows, extra_out = flip_allowance(wl, a, ref.a_rows)
+    ok_y, ey, ry = fp_tolerance_check(y, ref.y_rows, extra=e_rows)
+    assert ok_y, f"down rows: max|err| {ey:.4g} vs rms {ry:.4g}"
+    ok, err, rms = layer_tolerance_check(got, ref.out_f64, extra=extra_out)
+    assert ok, f"layer output: max|err| {err:.4g} vs rms {rms:.4g}"
